@@ -1,0 +1,267 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with what the pages or the mathematics fix.  They are chosen
+so that a plausible mistake anywhere in the oracle (a dropped term, a wrong
+sign, a swapped operand, a byte-order slip, an unstable sort) fails at least
+one of them; ``test_oracle_mutants.py`` plants such mistakes and checks that.
+
+Independent references used here: numpy's own float16 decoding, dense numpy /
+torch fp64 matmuls over all experts (brute force), scipy's expit, Python's
+stable ``sorted``, closed forms and the pages' printed byte sizes.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+from scipy.special import expit
+
+from routed_mixture_experts_router_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- helpers ----
+def np_dequant(blocks: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Independent Q8_0 decode with numpy's float16 (fp64 result)."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 34)
+    d = b[:, :2].copy().view("<f2").astype(np.float64)[:, 0]
+    q = b[:, 2:].copy().view(np.int8).astype(np.float64)
+    return (q * d[:, None]).reshape(rows, K)
+
+
+def tiny_layer(seed: int, T: int, dm: int, f: int, E: int, k: int, zipf: bool = False):
+    wl = synth.custom(f"tiny{seed}", wid=1000 + seed, T=T, d_model=dm, d_ff=f, E=E, k=k, zipf=zipf)
+    w = synth.make_layer(wl, 0, "cpu")
+    x = synth.make_x(wl, "cpu").double().numpy()
+    return wl, x, {kk: (None if v is None else v.numpy()) for kk, v in w.items()}
+
+
+def dense_bruteforce(x, Wr, bias, gate, up, down, dm, f, E, k, residual=False):
+    """All E experts for every token, full softmax, mask to top-k, renormalise, sum."""
+    Wg = np.stack([np_dequant(gate[e], f, dm) for e in range(E)])
+    Wu = np.stack([np_dequant(up[e], f, dm) for e in range(E)])
+    Wd = np.stack([np_dequant(down[e], dm, f) for e in range(E)])
+    logits = x @ Wr.astype(np.float64).T
+    if bias is not None:
+        logits = logits + bias.astype(np.float64)[None, :]
+    T = x.shape[0]
+    # full softmax over all experts
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    # top-k by (logit desc, id asc)
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((ids, -logits), axis=-1)
+    sel = order[:, :k]
+    mask = np.zeros((T, E))
+    np.put_along_axis(mask, sel, 1.0, axis=1)
+    wmix = p * mask
+    wmix /= wmix.sum(axis=1, keepdims=True)
+    G = np.einsum("efd,td->tef", Wg, x)
+    U = np.einsum("efd,td->tef", Wu, x)
+    H = G * expit(G) * U
+    Y = np.einsum("edf,tef->ted", Wd, H)
+    out = np.einsum("te,ted->td", wmix, Y)
+    if residual:
+        out = out + x
+    return out, sel.astype(np.int32), np.take_along_axis(wmix, sel, axis=1), logits
+
+
+def rel_l2_max(a, b):
+    num = np.linalg.norm(a - b, axis=-1)
+    den = np.maximum(np.linalg.norm(b, axis=-1), 1e-300)
+    return float((num / den).max())
+
+
+# ------------------------------------------------------------------- pins ----
+def pin_half_decode(orc):
+    """fp16 decode equals numpy's float16 for every non-NaN bit pattern."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    for bv in list(range(0, 65536, 97)) + [0, 1, 0x3ff, 0x400, 0x3c00, 0x7bff, 0x7c00, 0x8000, 0x8001, 0xfbff, 0xfc00]:
+        r = ref[bv]
+        got = orc.half_to_double(bv)
+        if np.isnan(r):
+            assert np.isnan(got), bv
+        else:
+            assert got == r, (hex(bv), got, r)
+
+
+def pin_q8_roundtrip(orc):
+    """Dequantise then re-encode reproduces the bytes (blocks containing |q|=127),
+    and every dequantised value is q*d of numpy's own decode."""
+    g = torch.Generator().manual_seed(7)
+    w = torch.randn(24, 96, generator=g) * 0.02
+    w[3, :32] = 0.0                       # an all-zero block
+    w[5, 32:64] *= 1e-3                   # small scales
+    blocks = synth.quantize_q8_0(w).numpy()
+    deq = orc.dequant_q8(blocks, 24, 96)
+    assert np.array_equal(deq, np_dequant(blocks, 24, 96))
+    again = synth.quantize_q8_0(torch.from_numpy(deq.astype(np.float32))).numpy()
+    assert np.array_equal(again, blocks)
+    assert np.all(deq[3, :32] == 0.0)
+    # every dequantised weight is exact in fp32 (8-bit q times 11-bit d)
+    assert np.array_equal(deq.astype(np.float32).astype(np.float64), deq)
+
+
+def pin_page_sizes(orc):
+    """The pages' printed expert-cache sizes follow from 34-byte Q8_0 blocks of
+    32 weights and three expert matrices of 2048 x 768.  The three matrices
+    come to 5,013,504 B (already a whole number of 4 KiB pages); the printed
+    raw-cache sizes and bytes-per-miss match that plus one more 4 KiB page per
+    page-aligned blob (the pages do not say what that page holds), and do not
+    match the bare 5,013,504 B (1536 slots would print 7.17 GiB)."""
+    bb, be = orc.q8_block_bytes(), orc.q8_block_elems()
+    expert = 3 * (2048 * 768 // be) * bb
+    assert expert == 5_013_504
+    assert expert % 4096 == 0
+    padded = expert + 4096
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "expert_cache_sizes.txt")) if ln.strip()
+            and not ln.startswith("#")]
+    for kind, *vals in rows:
+        if kind == "raw_cache_gib":
+            slots, gib = int(vals[0]), float(vals[1])
+            assert round(slots * padded / 2 ** 30, 2) == gib, (slots, gib)
+        elif kind == "miss_bytes":
+            misses, gb = int(vals[0]), float(vals[1])
+            per = gb * 1e9 / misses
+            assert abs(per - padded) / padded < 3e-3, (misses, per)
+        elif kind == "model_gb":
+            total = 48 * 128 * expert
+            assert round(total / 1e9) == int(vals[0])
+
+
+def pin_dense_bruteforce(orc):
+    """Sparse oracle == dense all-experts brute force (tiny shapes, several seeds)."""
+    for seed, (T, dm, f, E, k, zipf, res) in enumerate([
+        (4, 256, 128, 16, 2, False, False),    # the tiny workload's geometry
+        (5, 64, 32, 8, 3, True, False),
+        (3, 96, 64, 6, 6, False, True),         # k == E: full softmax mixture
+        (7, 32, 64, 12, 1, True, True),
+        (1, 64, 32, 4, 2, False, False),
+    ]):
+        wl, x, w = tiny_layer(seed, T, dm, f, E, k, zipf)
+        out, idx, wt, logits = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k,
+                                             residual=res)
+        ro, ridx, rw, rl = dense_bruteforce(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k,
+                                            residual=res)
+        assert np.allclose(logits, rl, rtol=0, atol=1e-12)
+        assert np.array_equal(idx, ridx), (seed, idx, ridx)
+        assert np.allclose(wt, rw, rtol=1e-12, atol=1e-15)
+        assert rel_l2_max(out, ro) < 1e-12, (seed, rel_l2_max(out, ro))
+
+
+def pin_k_equals_E_closed_form(orc):
+    """k = E: output is the full-softmax mixture of all experts (closed form)."""
+    T, dm, f, E = 3, 64, 32, 5
+    wl, x, w = tiny_layer(11, T, dm, f, E, E)
+    out, idx, wt, logits = orc.moe_layer(x, w["Wr"], None, w["gate"], w["up"], w["down"], dm, f, E, E)
+    lg = x @ w["Wr"].astype(np.float64).T
+    p = np.exp(lg - lg.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    ys = np.stack([[orc.expert_swiglu(w["gate"][e], w["up"][e], w["down"][e], dm, f, x[t]) for e in range(E)]
+                   for t in range(T)])
+    ref = np.einsum("te,ted->td", p, ys)
+    assert rel_l2_max(out, ref) < 1e-12
+    # every expert appears once per token, in descending-probability order
+    for t in range(T):
+        assert sorted(idx[t].tolist()) == list(range(E))
+        assert np.all(np.diff(wt[t]) <= 0)
+
+
+def pin_zero_input_ties(orc):
+    """x = 0, bias = 0: all logits tie at 0 -> experts 0..k-1, w = 1/k, output 0."""
+    T, dm, f, E, k = 3, 64, 32, 8, 3
+    wl, x, w = tiny_layer(3, T, dm, f, E, k)
+    x0 = np.zeros_like(x)
+    out, idx, wt, logits = orc.moe_layer(x0, w["Wr"], None, w["gate"], w["up"], w["down"], dm, f, E, k)
+    assert np.all(idx == np.arange(k)[None, :])
+    assert np.all(wt == 1.0 / k)
+    assert np.all(out == 0.0)
+
+
+def pin_weights_simplex(orc):
+    """Selected weights are positive, sum to 1 (1e-12) and descend; logits descend."""
+    T, dm, f, E, k = 16, 64, 32, 16, 4
+    wl, x, w = tiny_layer(5, T, dm, f, E, k, zipf=True)
+    out, idx, wt, logits = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k)
+    assert np.all(wt > 0)
+    assert np.allclose(wt.sum(1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(np.diff(wt, axis=1) <= 0)
+    sel_l = np.take_along_axis(logits, idx, axis=1)
+    assert np.all(np.diff(sel_l, axis=1) <= 0)
+    # the selected logits are the k largest
+    kth = np.sort(logits, axis=1)[:, ::-1][:, k - 1]
+    assert np.all(sel_l[:, -1] == kth)
+
+
+def pin_permutation_equivariance(orc):
+    """Permuting tokens permutes idx, w and out identically."""
+    T, dm, f, E, k = 9, 64, 32, 8, 2
+    wl, x, w = tiny_layer(9, T, dm, f, E, k, zipf=True)
+    perm = np.random.default_rng(3).permutation(T)
+    a = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k, residual=True)
+    b = orc.moe_layer(x[perm], w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k, residual=True)
+    assert np.array_equal(a[1][perm], b[1])
+    assert np.array_equal(a[2][perm], b[2])
+    assert np.array_equal(a[0][perm], b[0])
+
+
+def pin_single_expert_swiglu(orc):
+    """E = 1, k = 1 reduces to one SwiGLU FFN: torch fp64 matmuls + torch silu."""
+    T, dm, f, E, k = 4, 96, 64, 1, 1
+    wl, x, w = tiny_layer(13, T, dm, f, E, k)
+    out, idx, wt, _ = orc.moe_layer(x, w["Wr"], None, w["gate"], w["up"], w["down"], dm, f, E, k)
+    Wg = torch.from_numpy(np_dequant(w["gate"][0], f, dm))
+    Wu = torch.from_numpy(np_dequant(w["up"][0], f, dm))
+    Wd = torch.from_numpy(np_dequant(w["down"][0], dm, f))
+    xt = torch.from_numpy(x)
+    ref = (torch.nn.functional.silu(xt @ Wg.T) * (xt @ Wu.T)) @ Wd.T
+    assert np.all(idx == 0) and np.all(wt == 1.0)
+    assert rel_l2_max(out, ref.numpy()) < 1e-13
+
+
+def pin_bucket_bruteforce(orc):
+    """Bucketing == Python's stable sort of pairs by expert; sum of counts = T*k."""
+    rng = np.random.default_rng(5)
+    for T, k, E in [(1, 8, 128), (17, 3, 8), (64, 8, 128), (5, 2, 16), (0, 2, 4)]:
+        idx = np.array([rng.permutation(E)[:k] for _ in range(T)], dtype=np.int32).reshape(T, k)
+        if T >= 8:
+            idx[:4, 0] = 1          # a skewed expert
+        off, pt, ps, pos = orc.bucket(idx, E)
+        pairs = [(int(idx[t, s]), t, s) for t in range(T) for s in range(k)]
+        order = sorted(range(len(pairs)), key=lambda p: pairs[p][0])     # stable: ties keep (t, s) order
+        assert [pairs[p][1] for p in order] == pt.tolist()
+        assert [pairs[p][2] for p in order] == ps.tolist()
+        cnt = np.bincount(idx.reshape(-1), minlength=E) if T else np.zeros(E, np.int64)
+        assert off[0] == 0 and off[-1] == T * k
+        assert np.array_equal(np.diff(off), cnt)
+        for p_ in range(T * k):
+            assert pt[pos[p_]] == p_ // k and ps[pos[p_]] == p_ % k
+
+
+def pin_residual_stack(orc):
+    """With residual, out = x + MoE(x) exactly (same MoE term as without)."""
+    T, dm, f, E, k = 3, 64, 32, 8, 2
+    wl, x, w = tiny_layer(17, T, dm, f, E, k)
+    a = orc.moe_layer(x, w["Wr"], None, w["gate"], w["up"], w["down"], dm, f, E, k, residual=False)[0]
+    b = orc.moe_layer(x, w["Wr"], None, w["gate"], w["up"], w["down"], dm, f, E, k, residual=True)[0]
+    assert np.array_equal(b, x + a)
+    assert np.abs(a).max() > 0
+
+
+ALL_PINS = [
+    pin_half_decode,
+    pin_q8_roundtrip,
+    pin_page_sizes,
+    pin_dense_bruteforce,
+    pin_k_equals_E_closed_form,
+    pin_zero_input_ties,
+    pin_weights_simplex,
+    pin_permutation_equivariance,
+    pin_single_expert_swiglu,
+    pin_bucket_bruteforce,
+    pin_residual_stack,
+]
