@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MoE layer on GB300: MoE-layer tokens/s.
+
+Default workload: one qwen3_moe-geometry MoE layer at decode, T = 1 token
+(d_model 2048, d_ff 768, 128 experts, top-8, Q8_0 SwiGLU experts, fp32
+activations).  One step = one full layer forward (router, top-k, bucketing,
+gate/up, down + combine) through the C ABI, replayed from a CUDA graph.
+Steps rotate over R independently seeded layers (each with its own x), so the
+40 MB of expert weights a step touches are not L2-resident: the reuse
+distance is R-1 layers x 40 MB, far above the 129 MB L2.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle
+instead (the plain fp64 definition of the layer, on this host's cores).
+
+Multi-GPU: the layer has no exchange step at this scale, so N GPUs run N
+independent replicas (weak scaling); timing is barrier-bracketed and the
+max over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_mixture_experts_router_gb300 import binding, synth  # noqa: E402
+
+Q8_ROW_BYTES = lambda K: (K // 32) * 34  # noqa: E731  bytes of one Q8_0 row in HBM (int8 + fp16 per 32)
+
+
+def expert_bytes(wl) -> int:
+    """HBM bytes of one expert's three Q8_0 matrices (qs + scales)."""
+    return 2 * wl.d_ff * Q8_ROW_BYTES(wl.d_model) + wl.d_model * Q8_ROW_BYTES(wl.d_ff)
+
+
+# ------------------------------------------------------------------ dist ----
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int, device) -> float:
+    """Max of a host float over all ranks (timing only, not a data path)."""
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is under load."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for (t, p) in self.rows if t0 <= t <= t1] or [p for (_, p) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def cpu_info():
+    model = "unknown"
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return model, os.cpu_count()
+
+
+# ----------------------------------------------------------- CPU oracle ----
+def oracle_tokens_per_s(wl, layer_host, x_all: np.ndarray, budget_s: float = 12.0, max_s: float = 30.0):
+    """Time the fp64 oracle (as it stands) on batches of independent tokens of
+    the workload until ~budget_s of CPU work; returns (tokens/s, tokens, threads)."""
+    import oracle
+    orc = oracle.get()
+    threads = orc.num_threads()
+    batch = max(1, threads) * max(1, wl.T)
+    done, t_used = 0, 0.0
+    i = 0
+    while t_used < budget_s:
+        rows = np.arange(i, i + batch) % x_all.shape[0]
+        xb = x_all[rows]
+        t0 = time.perf_counter()
+        orc.moe_layer(xb, layer_host["Wr"], layer_host["bias"], layer_host["gate"], layer_host["up"],
+                      layer_host["down"], wl.d_model, wl.d_ff, wl.E, wl.k, residual=wl.residual)
+        t_used += time.perf_counter() - t0
+        done += batch
+        i += batch
+        if t_used > max_s:
+            break
+    return done / t_used, done, threads, t_used
+
+
+# ------------------------------------------------------------ reference ----
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    w = synth.make_layer(wl, 0, "cpu")
+    host = {k: (None if v is None else v.numpy()) for k, v in w.items()}
+    import oracle
+    orc = oracle.get()
+    threads = orc.num_threads()
+    per_step = max(1, threads)           # independent decode tokens per step, one per core
+    xs = synth.make_x(wl, "cpu", step=0, T=per_step * (args.steps + args.warmup)).double().numpy()
+
+    def step(i):
+        xb = xs[i * per_step:(i + 1) * per_step]
+        orc.moe_layer(xb, host["Wr"], host["bias"], host["gate"], host["up"], host["down"], wl.d_model, wl.d_ff,
+                      wl.E, wl.k, residual=wl.residual)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * per_step
+    value = tokens / dt
+    model, ncpu = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, qwen3_moe geometry)",
+        "config": workload_config(wl, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} steps x {per_step} independent T=1 tokens, layer 0, "
+                                   f"{model}, {ncpu} host cores"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "MoE-layer tokens/s (decode T=1/64, prefill T=1024); HBM GB/s & TC % of peak"
+
+
+def workload_config(wl, args):
+    return {"workload": f"{wl.name}: one MoE layer, T={wl.T}, d_model={wl.d_model}, d_ff={wl.d_ff}, E={wl.E}, "
+                        f"top-{wl.k}, Q8_0 SwiGLU experts, {wl.act} activations",
+            "tokens_per_step": wl.T, "layers_rotated": args.rot,
+            "l2": f"inputs larger than L2: steps rotate over {args.rot} seeded layers "
+                  f"({args.rot} x {wl.E} experts x {expert_bytes(wl)} B resident)",
+            "parallelism": f"replicas x{args.gpus}", "graph": "one CUDA graph per step (layer forward)"}
+
+
+# ------------------------------------------------------------------ ours ----
+def run_ours(args, ws, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
+    if act != binding.MOE_ACT_F32:
+        raise SystemExit("only the fp32-activation workloads are wired into this benchmark")
+    binding.load()
+    R = args.rot
+    layers, xs, outs, wss = [], [], [], []
+    host0 = None
+    for r in range(R):
+        w = synth.make_layer(wl, r, dev)
+        if r == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
+        layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
+                                                w["Wr"], w["bias"]))
+        del w
+        xs.append(synth.make_x(wl, dev, step=r))
+        outs.append(torch.empty(wl.T, wl.d_model, dtype=torch.float32, device=dev))
+        wss.append(binding.workspace(wl.T, layers[-1], act, 0, dev))
+    torch.cuda.synchronize()
+    P = wl.T * wl.k
+    # split buffers for the per-kernel (expert FFN) timing pass
+    idxs = [torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev) for _ in range(R)]
+    wtss = [torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev) for _ in range(R)]
+    offs = [torch.empty(wl.E + 1, dtype=torch.int32, device=dev) for _ in range(R)]
+    pts = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
+    pss = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
+    poss = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
+    outs2 = [torch.empty_like(o) for o in outs]
+
+    stream = torch.cuda.Stream(device=dev)
+    L = binding.load()
+    st = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
+
+    def step_call(r):
+        binding.layer_forward(xs[r], layers[r], act, 0, wl.residual, out=outs[r], ws=wss[r])
+
+    def rb_call(r):
+        binding._check("moe_route", L.moe_route(binding._ptr(xs[r]), wl.T, layers[r].ref(), binding._ptr(idxs[r]),
+                                                binding._ptr(wtss[r]), binding.ctypes.c_void_p(st())))
+        binding._check("moe_bucket", L.moe_bucket(binding._ptr(idxs[r]), wl.T, wl.k, wl.E, binding._ptr(offs[r]),
+                                                  binding._ptr(pts[r]), binding._ptr(pss[r]), binding._ptr(poss[r]),
+                                                  None, binding.ctypes.c_void_p(st())))
+
+    def ffn_call(r):
+        binding.expert_ffn_q8(xs[r], layers[r], offs[r], pts[r], pss[r], wtss[r], act, True, wl.residual,
+                              ws=wss[r], out=outs2[r])
+
+    # eager warm-up (also sets kernel attributes outside capture), then capture
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            step_call(r)
+            rb_call(r)
+            ffn_call(r)
+    torch.cuda.synchronize()
+    g_step, g_rb, g_ffn = [], [], []
+    for r in range(R):
+        for lst, fn in ((g_step, step_call), (g_rb, rb_call), (g_ffn, ffn_call)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(r)
+            lst.append(g)
+    torch.cuda.synchronize()
+
+    # distinct experts per rotation slot (for the algorithmic bytes)
+    n_active = []
+    for r in range(R):
+        o = offs[r].cpu().numpy()
+        n_active.append(int((np.diff(o) > 0).sum()))
+    xbytes = wl.T * wl.d_model * 4
+    ffn_bytes = [n * expert_bytes(wl) + 2 * xbytes for n in n_active]        # weights + x in + out
+    step_bytes = [b + wl.E * wl.d_model * 4 + (wl.E * 4 if wl.zipf else 0) for b in ffn_bytes]  # + router
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            g_step[i % R].replay()
+        torch.cuda.synchronize()
+        # soak: keep the GPU busy ~1 s so the sampled clocks reflect load
+        t_soak = time.time()
+        i = 0
+        while time.time() - t_soak < args.soak:
+            for _ in range(200):
+                g_step[i % R].replay()
+                i += 1
+            torch.cuda.synchronize()
+        t_clk0 = time.time()
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            g_step[i % R].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        t_clk1 = time.time()
+    ms_local = e0.elapsed_time(e1)
+    sampler.stop()
+    clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
+    ms = max_over_ranks(ms_local, ws, dev)
+    tokens = args.steps * wl.T * ws
+    value = tokens / (ms / 1e3)
+
+    # per-kernel pass: events around the expert FFN (gate/up + down) on the launch stream
+    with torch.cuda.stream(stream):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            r = i % R
+            g_rb[r].replay()
+            evs[i][0].record(stream)
+            g_ffn[r].replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    ffn_ms = [a.elapsed_time(b) for a, b in evs]
+    ffn_ms_mean = float(np.mean(ffn_ms))
+    ffn_alg = float(np.mean([ffn_bytes[i % R] for i in range(args.steps)]))
+    peaks = load_peaks()
+    achieved = ffn_alg / (ffn_ms_mean / 1e3) / 1e9
+    roofline = {"kernel": "moe_expert_ffn_q8 (gate/up + down, Q8_0 fused, combine fused)",
+                "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": ffn_alg, "launch_ms": ffn_ms_mean,
+                "traffic": args.traffic}
+    step_alg = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
+    layer_gbs = step_alg / (ms_local / args.steps / 1e3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = torch.empty(wl.T, wl.d_model, dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            r = i % R
+            xs[r].copy_(xh[r], non_blocking=True)
+            g_step[r].replay()
+            oh.copy_(outs[r], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+    e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
+           "d2h_bytes_per_step": xbytes}
+
+    cpu_base = None
+    if host0 is not None:
+        xa = synth.make_x(wl, "cpu", step=1000, T=256).double().numpy()
+        tps, done, threads, secs = oracle_tokens_per_s(wl, host0, xa, budget_s=args.cpu_budget)
+        model, ncpu = cpu_info()
+        cpu_base = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                    "sample": f"{done} independent T={wl.T} tokens of layer 0 in {secs:.1f} s "
+                              f"(batches of {threads}), {model}, {ncpu} host cores"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, qwen3_moe geometry, random-init Q8_0)",
+            "config": workload_config(wl, args),
+            "layer_hbm_gbs": layer_gbs, "near_ties": None,
+            "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--rot", type=int, default=16, help="seeded layers the steps rotate over")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the timed kernel from an ncu capture of this build")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ws, rank)
+        return run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

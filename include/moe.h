@@ -1,0 +1,189 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300.so: a routed Mixture-of-Experts layer with
+ * Q8_0 SwiGLU experts, hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (qwen3_moe geometry: d_model 2048, d_ff 768, 128 experts, top-8,
+ * 48 layers -- amalgafy.com/evidence, "Historical baseline environment"):
+ *
+ *   router   l[t][e] = x[t] . Wr[e] (+ bias[e])        "LinearGate" routing,
+ *                                                        amalgafy.com/evidence
+ *   top-k    the k largest logits, ties to the lower expert id, ordered by
+ *            descending logit; weights w_i = exp(l_i - l_max) / sum_sel exp(.)
+ *            ("GPU router/top-k", amalgafy.com/technical-overview)
+ *   bucket   (token, slot) pairs grouped by expert, stable in (token, slot)
+ *            order ("compact expert grouping", expxa.com
+ *            reuse-ordering-qualification, "What changed from the first
+ *            experiment")
+ *   experts  y = Wd (silu(Wg x) * (Wu x)), every weight Q8_0-dequantised as
+ *            w = q * d (native Q8_0 weights, amalgafy.com/technical-overview,
+ *            "Validated GPU foundation"; down projection K=768 -> 2048 rows,
+ *            expxa.com, "What changed from the first experiment")
+ *   combine  out[t] = (residual ? x[t] : 0) + sum_slot w[t][slot] * y
+ *            ("weighted combine", amalgafy.com/technical-overview,
+ *            "Execution architecture")
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated
+ *    otherwise.  The library allocates no device memory: scratch comes from a
+ *    caller workspace sized by moe_workspace_size().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on it: it never synchronises the
+ *    device or the stream and never reads results back to the host.
+ *  - The return value is a MOE_* code.  Host-side argument checks run before
+ *    anything is enqueued; MOE_ERR_CUDA reports a launch error.
+ *  - Problems the device finds (an expert id out of range, a duplicate id in
+ *    one token's selection) are OR-ed into an optional caller-owned int32
+ *    status word (MOE_STATUS_*); the caller reads it whenever it likes.
+ *  - The library holds no per-call state; calls on different streams with
+ *    different buffers may run concurrently.
+ *  - Alignment: every float / int32 array 16-byte aligned; qs and d arrays
+ *    16-byte aligned; d_model and d_ff multiples of 32.
+ *
+ * Device weight layout (produced by moe_pack_q8 from the 34-byte blocks):
+ *   qs  int8     [E][rows][K]       the 32 int8 values of each block, along K
+ *   d   fp16 bits[E][rows][K/32]    one scale per 32-wide block
+ *   gate, up: rows = d_ff, K = d_model;  down: rows = d_model, K = d_ff.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1  /* null/misaligned pointer, bad size, k > E, ... */
+#define MOE_ERR_UNSUPPORTED 2  /* device is not sm_100/sm_103, or a mode not built */
+#define MOE_ERR_CUDA 3         /* a launch failed (cudaGetLastError) */
+#define MOE_ERR_WORKSPACE 4    /* workspace null or smaller than moe_workspace_size() */
+
+/* ---- device status bits (OR-ed into *status) ------------------------- */
+#define MOE_STATUS_BAD_INDEX 1 /* an expert id outside [0, E), or repeated in one token */
+
+/* ---- expert-input precision ------------------------------------------ */
+#define MOE_ACT_F32 0  /* fp32 activations, CUDA-core Q8_0 contraction (decode) */
+#define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill) */
+
+/* ---- flags ----------------------------------------------------------- */
+#define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */
+
+/* Limits: E <= 256, k <= 32, k <= E, d_model and d_ff multiples of 32,
+ * d_model <= 8192, d_ff <= 8192, T <= 65536. */
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 32
+
+/* One Q8_0 matrix family (all E experts), device layout above. */
+typedef struct {
+    const int8_t* qs;
+    const uint16_t* d;
+} moe_q8_mat;
+
+/* One layer's weights.  router_w: fp32 [E][d_model]; router_bias: fp32 [E]
+ * or NULL. */
+typedef struct {
+    int E, k, d_model, d_ff;
+    moe_q8_mat gate, up, down;
+    const float* router_w;
+    const float* router_bias;
+} moe_layer_w;
+
+/*
+ * Bytes of workspace the calls below need for T tokens (0 if the arguments
+ * are invalid).  act: MOE_ACT_*; flags: MOE_FLAG_*.  The workspace must be
+ * 256-byte aligned.  It holds the routing results, the bucketing, the SwiGLU
+ * activations h and, for MOE_FLAG_DETERMINISTIC, the per-pair outputs.
+ */
+MOE_API size_t moe_workspace_size(int T, const moe_layer_w* w, int act, int flags);
+
+/*
+ * Repack Q8_0 weights from the pages' 34-byte blocks (fp16 scale d, little
+ * endian, then 32 int8 values q along K) into the device layout.
+ *   blocks: device bytes, rows * (K/32) blocks, row-major (any alignment)
+ *   qs: int8 [rows][K] (16-byte aligned); d: fp16 bits [rows][K/32]
+ * rows may span several experts ([E*rows_per_expert]).  Bit-exact copy.
+ */
+MOE_API int moe_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, void* stream);
+
+/*
+ * Router: logits x . Wr^T (+ bias) in fp32, top-k (ties to the lower id,
+ * descending logit), renormalised softmax weights.
+ *   x: fp32 [T][d_model]; idx: int32 [T][k]; wts: fp32 [T][k].
+ * Deterministic: the same inputs give bit-identical idx and wts.
+ */
+MOE_API int moe_route(const float* x, int T, const moe_layer_w* w, int32_t* idx, float* wts, void* stream);
+
+/*
+ * Compact expert grouping: a stable counting sort of the T*k pairs by expert.
+ *   idx: int32 [T][k] expert ids.
+ *   offsets: int32 [E+1], offsets[e] = number of pairs with expert < e
+ *   pair_tok, pair_slot: int32 [T*k], the pairs in bucket order, ascending
+ *       (token, slot) within one expert
+ *   pos: int32 [T*k], pos[t*k+s] = bucket position of pair (t, s)
+ *   status: optional; MOE_STATUS_BAD_INDEX if an id is out of range or
+ *       repeated within a token (such pairs are dropped; outputs then only
+ *       stay in bounds)
+ * Deterministic (no atomics decide any position).
+ */
+MOE_API int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
+               int32_t* pos, int32_t* status, void* stream);
+
+/*
+ * Expert SwiGLU FFNs over the bucketed pairs, Q8_0 dequantisation fused into
+ * the contractions.
+ *   x: fp32 [T][d_model] expert inputs (token-indexed)
+ *   offsets, pair_tok, pair_slot, pos, wts: from moe_bucket / moe_route
+ *   act: MOE_ACT_F32 (fp32 FMA) or MOE_ACT_BF16 (tcgen05, bf16 operands,
+ *        fp32 accumulation)
+ *   fuse_combine = 1: out_or_ypairs is out fp32 [T][d_model]; it is
+ *        overwritten with (residual ? x : 0) + sum_slot w * y (fp32 atomic
+ *        adds, so the last bits may vary run to run)
+ *   fuse_combine = 0: out_or_ypairs is ypairs fp32 [T*k][d_model], row p
+ *        holding y of the pair in bucket position p (bit-reproducible);
+ *        `residual` is ignored.  Combine with moe_combine().
+ *   ws / ws_bytes: workspace of at least moe_workspace_size(T, w, act, 0).
+ * out must not alias x.
+ */
+MOE_API int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t* offsets, const int32_t* pair_tok,
+                      const int32_t* pair_slot, const float* wts, int act, int fuse_combine, float* out_or_ypairs,
+                      int residual, void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Weighted combine in a fixed order (bit-reproducible):
+ *   out[t][o] = (residual ? residual[t][o] : 0) + sum_{s=0..k-1} wts[t][s] * ypairs[pos[t*k+s]][o]
+ *   ypairs fp32 [T*k][d_model]; residual fp32 [T][d_model] or NULL.
+ */
+MOE_API int moe_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int d_model,
+                const float* residual, float* out, void* stream);
+
+/*
+ * The whole layer: route -> bucket -> gate/up -> down + combine.
+ *   x: fp32 [T][d_model]; out: fp32 [T][d_model], must not alias x
+ *   act: MOE_ACT_F32 or MOE_ACT_BF16; flags: MOE_FLAG_*
+ *   residual: 1 adds x to the output (a residual stream between layers)
+ *   idx_out [T][k], wts_out [T][k], offsets_out [E+1]: optional copies of the
+ *       routing and bucketing (NULL to skip)
+ *   ws / ws_bytes: at least moe_workspace_size(T, w, act, flags)
+ * Enqueues a fixed sequence of kernels (no host synchronisation), so the call
+ * can be captured into a CUDA graph and replayed.
+ */
+MOE_API int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual, float* out,
+                      int32_t* idx_out, float* wts_out, int32_t* offsets_out, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream);
+
+/* Library version string (static storage). */
+MOE_API const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libmoe_gb300.so (C ABI declared in include/moe.h).
+
+Argument marshalling only: every function passes torch tensors' device
+pointers and the current CUDA stream to the C entry point of the same name,
+and raises ``MoeError`` on a non-zero return code.  No computation happens in
+Python, and there is no fallback: if the library is missing or fails to load,
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_WORKSPACE = 4
+MOE_STATUS_BAD_INDEX = 1
+MOE_ACT_F32 = 0
+MOE_ACT_BF16 = 1
+MOE_FLAG_DETERMINISTIC = 1
+
+_ERR = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE"}
+
+ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
+                "moe_layer_forward", "moe_version")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, rc: int):
+        super().__init__(f"{fn} returned {rc} ({_ERR.get(rc, 'unknown')})")
+        self.rc = rc
+
+
+class Q8Mat(ctypes.Structure):
+    _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p)]
+
+
+class LayerW(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("k", ctypes.c_int), ("d_model", ctypes.c_int), ("d_ff", ctypes.c_int),
+                ("gate", Q8Mat), ("up", Q8Mat), ("down", Q8Mat), ("router_w", ctypes.c_void_p),
+                ("router_bias", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load the library (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe_gb300.so not found at {path}; build it with "
+                           "`python -m routed_mixture_experts_router_gb300.build`")
+    L = ctypes.CDLL(path)
+    P, I, LL, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+    LWP = ctypes.POINTER(LayerW)
+    L.moe_workspace_size.restype = SZ
+    L.moe_workspace_size.argtypes = [I, LWP, I, I]
+    L.moe_pack_q8.restype = I
+    L.moe_pack_q8.argtypes = [P, LL, I, P, P, P]
+    L.moe_route.restype = I
+    L.moe_route.argtypes = [P, I, LWP, P, P, P]
+    L.moe_bucket.restype = I
+    L.moe_bucket.argtypes = [P, I, I, I, P, P, P, P, P, P]
+    L.moe_expert_ffn_q8.restype = I
+    L.moe_expert_ffn_q8.argtypes = [P, I, LWP, P, P, P, P, I, I, P, I, P, SZ, P, P]
+    L.moe_combine.restype = I
+    L.moe_combine.argtypes = [P, P, P, I, I, I, P, P, P]
+    L.moe_layer_forward.restype = I
+    L.moe_layer_forward.argtypes = [P, I, LWP, I, I, I, P, P, P, P, P, SZ, P, P]
+    L.moe_version.restype = ctypes.c_char_p
+    L.moe_version.argtypes = []
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+class Layer:
+    """Device-resident weights of one MoE layer in the library's layout.
+
+    Holds the packed Q8_0 tensors (qs int8 [E][rows][K], d fp16-bits
+    [E][rows][K/32]) and the fp32 router, plus the C struct pointing at them.
+    """
+
+    def __init__(self, E, k, d_model, d_ff, gate, up, down, router_w, router_bias=None):
+        self.E, self.k, self.d_model, self.d_ff = E, k, d_model, d_ff
+        self.gate, self.up, self.down = gate, up, down          # (qs, d) tuples
+        self.router_w = router_w.contiguous()
+        self.router_bias = None if router_bias is None else router_bias.contiguous()
+        self.c = LayerW(E, k, d_model, d_ff, Q8Mat(gate[0].data_ptr(), gate[1].data_ptr()),
+                        Q8Mat(up[0].data_ptr(), up[1].data_ptr()), Q8Mat(down[0].data_ptr(), down[1].data_ptr()),
+                        self.router_w.data_ptr(), 0 if self.router_bias is None else self.router_bias.data_ptr())
+
+    @classmethod
+    def from_blocks(cls, E, k, d_model, d_ff, gate_blocks, up_blocks, down_blocks, router_w, router_bias=None):
+        """Pack the pages' 34-byte Q8_0 blocks (device uint8 tensors) with moe_pack_q8."""
+        gate = pack_q8(gate_blocks, E * d_ff, d_model)
+        up = pack_q8(up_blocks, E * d_ff, d_model)
+        down = pack_q8(down_blocks, E * d_model, d_ff)
+        return cls(E, k, d_model, d_ff, gate, up, down, router_w, router_bias)
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def version() -> str:
+    return load().moe_version().decode()
+
+
+def pack_q8(blocks: torch.Tensor, rows: int, K: int):
+    """moe_pack_q8: 34-byte blocks -> (qs int8 [rows][K], d int16-bits [rows][K/32])."""
+    L = load()
+    qs = torch.empty(rows, K, dtype=torch.int8, device=blocks.device)
+    d = torch.empty(rows, K // 32, dtype=torch.int16, device=blocks.device)
+    _check("moe_pack_q8", L.moe_pack_q8(_ptr(blocks), rows, K, _ptr(qs), _ptr(d), _stream()))
+    return qs, d
+
+
+def workspace_size(T: int, layer: Layer, act: int = MOE_ACT_F32, flags: int = 0) -> int:
+    return int(load().moe_workspace_size(T, layer.ref(), act, flags))
+
+
+def workspace(T: int, layer: Layer, act: int = MOE_ACT_F32, flags: int = 0, device="cuda") -> torch.Tensor:
+    n = workspace_size(T, layer, act, flags)
+    if n == 0 and T > 0:
+        raise MoeError("moe_workspace_size", MOE_ERR_INVALID_ARG)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def route(x: torch.Tensor, layer: Layer):
+    T = x.shape[0]
+    idx = torch.empty(T, layer.k, dtype=torch.int32, device=x.device)
+    wts = torch.empty(T, layer.k, dtype=torch.float32, device=x.device)
+    _check("moe_route", load().moe_route(_ptr(x), T, layer.ref(), _ptr(idx), _ptr(wts), _stream()))
+    return idx, wts
+
+
+def bucket(idx: torch.Tensor, E: int, status: torch.Tensor | None = None):
+    T, k = idx.shape
+    dev = idx.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    pair_tok = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    pair_slot = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    pos = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    _check("moe_bucket", load().moe_bucket(_ptr(idx), T, k, E, _ptr(offsets), _ptr(pair_tok), _ptr(pair_slot),
+                                           _ptr(pos), _ptr(status), _stream()))
+    return offsets, pair_tok[:T * k], pair_slot[:T * k], pos[:T * k]
+
+
+def expert_ffn_q8(x, layer: Layer, offsets, pair_tok, pair_slot, wts, act=MOE_ACT_F32, fuse_combine=True,
+                  residual=False, ws=None, status=None, out=None):
+    T = x.shape[0]
+    if out is None:
+        rows = T if fuse_combine else T * layer.k
+        out = torch.empty(rows, layer.d_model, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(T, layer, act, 0, x.device)
+    _check("moe_expert_ffn_q8", load().moe_expert_ffn_q8(
+        _ptr(x), T, layer.ref(), _ptr(offsets), _ptr(pair_tok), _ptr(pair_slot), _ptr(wts), act,
+        int(bool(fuse_combine)), _ptr(out), int(bool(residual)), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+    return out
+
+
+def combine(ypairs, wts, pos, T: int, k: int, d_model: int, residual=None, out=None):
+    if out is None:
+        out = torch.empty(T, d_model, dtype=torch.float32, device=ypairs.device)
+    _check("moe_combine", load().moe_combine(_ptr(ypairs), _ptr(wts), _ptr(pos), T, k, d_model, _ptr(residual),
+                                             _ptr(out), _stream()))
+    return out
+
+
+def layer_forward(x, layer: Layer, act=MOE_ACT_F32, flags=0, residual=False, out=None, ws=None, status=None,
+                  idx_out=None, wts_out=None, offsets_out=None):
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, layer.d_model, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(T, layer, act, flags, x.device)
+    _check("moe_layer_forward", load().moe_layer_forward(
+        _ptr(x), T, layer.ref(), act, flags, int(bool(residual)), _ptr(out), _ptr(idx_out), _ptr(wts_out),
+        _ptr(offsets_out), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+    return out

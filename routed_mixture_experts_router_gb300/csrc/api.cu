@@ -1,0 +1,203 @@
+// C ABI of libmoe_gb300: argument checks, workspace carving and the launch
+// sequence of the routed MoE layer.  Every entry point only enqueues work on
+// the caller's stream; nothing here synchronises or reads back.
+#include <limits.h>
+
+#include "common.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct WsLayout {
+    size_t idx, wts, off, ptok, pslot, pos, h, ypairs, total;
+};
+
+// Workspace carve-up shared by every entry point: the routing results, the
+// bucketing, the SwiGLU activations h [P][d_ff] and, for the deterministic
+// combine, the per-pair outputs [P][d_model].
+WsLayout ws_layout(int T, const moe_layer_w& w, int act, int flags) {
+    const size_t P = (size_t)T * w.k;
+    WsLayout L{};
+    size_t o = 0;
+    L.idx = o;    o = align_up(o + P * sizeof(int32_t));
+    L.wts = o;    o = align_up(o + P * sizeof(float));
+    L.off = o;    o = align_up(o + (size_t)(w.E + 1) * sizeof(int32_t));
+    L.ptok = o;   o = align_up(o + P * sizeof(int32_t));
+    L.pslot = o;  o = align_up(o + P * sizeof(int32_t));
+    L.pos = o;    o = align_up(o + P * sizeof(int32_t));
+    L.h = o;      o = align_up(o + P * (size_t)w.d_ff * sizeof(float));
+    L.ypairs = o;
+    if (flags & MOE_FLAG_DETERMINISTIC) o = align_up(o + P * (size_t)w.d_model * sizeof(float));
+    L.total = o;
+    (void)act;
+    return L;
+}
+
+bool valid_geometry(const moe_layer_w* w) {
+    if (!w) return false;
+    if (w->E < 1 || w->E > MOE_MAX_EXPERTS) return false;
+    if (w->k < 1 || w->k > MOE_MAX_TOPK || w->k > w->E) return false;
+    if (w->d_model < 32 || w->d_model % 32 || w->d_model > 8192) return false;
+    if (w->d_ff < 32 || w->d_ff % 32 || w->d_ff > 8192) return false;
+    return true;
+}
+
+bool valid_T(int T, const moe_layer_w* w) { return T >= 0 && T <= 65536 && (long long)T * w->k <= INT_MAX / 2; }
+
+bool valid_router(const moe_layer_w* w) {
+    return w->router_w && aligned16(w->router_w) && (!w->router_bias || aligned16(w->router_bias));
+}
+
+bool valid_experts(const moe_layer_w* w) {
+    const moe_q8_mat* m[3] = {&w->gate, &w->up, &w->down};
+    for (auto* q : m)
+        if (!q->qs || !q->d || !aligned16(q->qs) || !aligned16(q->d)) return false;
+    return true;
+}
+
+// sm_103 (GB300) only: the library is built for sm_103a.
+int check_device() {
+    static int cached[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    if (cached[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return cached[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+inline int cuda_rc(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
+
+size_t moe_workspace_size(int T, const moe_layer_w* w, int act, int flags) {
+    if (!valid_geometry(w) || !valid_T(T, w)) return 0;
+    if (act != MOE_ACT_F32 && act != MOE_ACT_BF16) return 0;
+    return ws_layout(T, *w, act, flags).total;
+}
+
+int moe_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, void* stream) {
+    if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !qs || !d || !aligned16(qs)) return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_pack_q8(blocks, rows, K, qs, d, (cudaStream_t)stream));
+}
+
+int moe_route(const float* x, int T, const moe_layer_w* w, int32_t* idx, float* wts, void* stream) {
+    if (!valid_geometry(w) || !valid_T(T, w)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !idx || !wts || !aligned16(x) || !valid_router(w)) return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_route(x, T, *w, idx, wts, (cudaStream_t)stream));
+}
+
+int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
+               int32_t* pos, int32_t* status, void* stream) {
+    if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_TOPK || k > E || T < 0 || T > 65536)
+        return MOE_ERR_INVALID_ARG;
+    if (!offsets || (T > 0 && (!idx || !pair_tok || !pair_slot || !pos))) return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_bucket(idx, T, k, E, offsets, pair_tok, pair_slot, pos, status, (cudaStream_t)stream));
+}
+
+int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t* offsets, const int32_t* pair_tok,
+                      const int32_t* pair_slot, const float* wts, int act, int fuse_combine, float* out_or_ypairs,
+                      int residual, void* ws, size_t ws_bytes, int32_t* status, void* stream) {
+    (void)status;
+    if (!valid_geometry(w) || !valid_T(T, w)) return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_F32 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !offsets || !pair_tok || !pair_slot || !wts || !out_or_ypairs || !aligned16(x) ||
+        !aligned16(out_or_ypairs) || !valid_experts(w))
+        return MOE_ERR_INVALID_ARG;
+    if (fuse_combine && (const void*)out_or_ypairs == (const void*)x) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, *w, act, 0);
+    if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc) return rc;
+    if (act != MOE_ACT_F32) return MOE_ERR_UNSUPPORTED;
+    char* base = static_cast<char*>(ws);
+    return cuda_rc(launch_ffn_f32(x, T, *w, offsets, pair_tok, pair_slot, wts, fuse_combine ? 1 : 0, out_or_ypairs,
+                                  residual, reinterpret_cast<float*>(base + L.h), (cudaStream_t)stream));
+}
+
+int moe_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int d_model,
+                const float* residual, float* out, void* stream) {
+    if (T < 0 || k < 1 || k > MOE_MAX_TOPK || d_model < 32 || d_model % 32) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!ypairs || !wts || !pos || !out || !aligned16(ypairs) || !aligned16(out) ||
+        (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_combine(ypairs, wts, pos, T, k, d_model, residual, out, (cudaStream_t)stream));
+}
+
+int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual, float* out,
+                      int32_t* idx_out, float* wts_out, int32_t* offsets_out, void* ws, size_t ws_bytes,
+                      int32_t* status, void* stream) {
+    if (!valid_geometry(w) || !valid_T(T, w)) return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_F32 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !out || !aligned16(x) || !aligned16(out) || (const void*)x == (const void*)out || !valid_router(w) ||
+        !valid_experts(w))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, *w, act, flags);
+    if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc) return rc;
+    if (act != MOE_ACT_F32) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = static_cast<char*>(ws);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.idx);
+    float* wts = wts_out ? wts_out : reinterpret_cast<float*>(base + L.wts);
+    int32_t* off = offsets_out ? offsets_out : reinterpret_cast<int32_t*>(base + L.off);
+    int32_t* ptok = reinterpret_cast<int32_t*>(base + L.ptok);
+    int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
+    int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
+    float* h = reinterpret_cast<float*>(base + L.h);
+    cudaError_t e = launch_route(x, T, *w, idx, wts, s);
+    if (e != cudaSuccess) return cuda_rc(e);
+    e = launch_bucket(idx, T, w->k, w->E, off, ptok, pslot, pos, status, s);
+    if (e != cudaSuccess) return cuda_rc(e);
+    if (flags & MOE_FLAG_DETERMINISTIC) {
+        float* yp = reinterpret_cast<float*>(base + L.ypairs);
+        e = launch_ffn_f32(x, T, *w, off, ptok, pslot, wts, 0, yp, 0, h, s);
+        if (e != cudaSuccess) return cuda_rc(e);
+        e = launch_combine(yp, wts, pos, T, w->k, w->d_model, residual ? x : nullptr, out, s);
+    } else {
+        e = launch_ffn_f32(x, T, *w, off, ptok, pslot, wts, 1, out, residual, h, s);
+    }
+    return cuda_rc(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// Compact expert grouping: a stable counting sort of the T*k (token, slot)
+// pairs by expert id ("compact expert grouping", expxa.com
+// reuse-ordering-qualification, "What changed from the first experiment").
+//
+// The pages report shared-memory race warnings in their grouping helper
+// ("Why it was not adopted"); this one decides every position without
+// atomics, so it is deterministic and race-free by construction:
+//   1. counts per expert (shared-memory atomics: order-free integer adds),
+//      exclusive scan -> offsets;
+//   2. tokens in chunks of 1024, one token per thread.  A token's experts
+//      form a bitmap over E; warp ballots transpose the bitmaps so that lane
+//      b of warp w holds M[w][e] = the set of lanes (tokens) of warp w that
+//      picked expert e.  The rank of token t in bucket e is
+//        (pairs of e in earlier chunks) + (popcounts of M[w'][e], w' < w)
+//        + popc(M[w][e] & lanes below t).
+//      Since one token picks each expert at most once, ascending token order
+//      is ascending (token, slot) order within a bucket.
+// Single CTA: the work is T*k integers; latency, not bandwidth, matters.
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBucketThreads = 1024;
+constexpr int kBucketWarps = kBucketThreads / kWarp;
+
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                                int32_t* __restrict__ offsets,
+                                                                int32_t* __restrict__ pair_tok,
+                                                                int32_t* __restrict__ pair_slot,
+                                                                int32_t* __restrict__ pos, int32_t* status) {
+    __shared__ int s_cnt[MOE_MAX_EXPERTS];
+    __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+    __shared__ int s_run[MOE_MAX_EXPERTS];   // pairs placed by earlier chunks
+    __shared__ int s_scan[MOE_MAX_EXPERTS];
+    __shared__ int s_bad;
+    extern __shared__ uint32_t bucket_dyn[];
+    const int words = (E + 31) >> 5;
+    const int ep = words * 32;
+    uint32_t* s_mask = bucket_dyn;                                   // M[w][e], [32][ep]
+    int* s_base = reinterpret_cast<int*>(bucket_dyn + kBucketWarps * ep);  // rank base of warp w in bucket e
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid < MOE_MAX_EXPERTS) {
+        s_cnt[tid] = 0;
+        s_run[tid] = 0;
+    }
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // 1. counts (valid ids only; a repeated id within a token is dropped below
+    //    and not counted: rows with repeats are detected per token)
+    for (int t = tid; t < T; t += kBucketThreads) {
+        uint32_t bm[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
+        for (int s = 0; s < k; ++s) {
+            const int e = __ldg(idx + (size_t)t * k + s);
+            if (e < 0 || e >= E) {
+                s_bad = 1;
+                continue;
+            }
+            const uint32_t bit = 1u << (e & 31);
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                if (j == (e >> 5)) word = bm[j];
+            if (word & bit) {
+                s_bad = 1;
+                continue;
+            }
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                if (j == (e >> 5)) bm[j] |= bit;
+            atomicAdd(&s_cnt[e], 1);
+        }
+    }
+    __syncthreads();
+    // exclusive scan over E <= 256 counts: warps 0..7 scan 32 each, then fix up
+    if (tid < MOE_MAX_EXPERTS) {
+        int v = tid < E ? s_cnt[tid] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        s_scan[tid] = incl;  // inclusive within its warp
+    }
+    __syncthreads();
+    if (tid < MOE_MAX_EXPERTS) {
+        int add = 0;
+        for (int w = 0; w < (tid >> 5); ++w) add += s_scan[w * 32 + 31];
+        const int incl = s_scan[tid] + add;
+        const int v = tid < E ? s_cnt[tid] : 0;
+        if (tid < E) s_off[tid] = incl - v;
+        if (tid == E - 1) s_off[E] = incl;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += kBucketThreads) offsets[e] = s_off[e];
+
+    // 2. stable scatter, 1024 tokens per chunk
+    for (int c0 = 0; c0 < T; c0 += kBucketThreads) {
+        const int t = c0 + tid;
+        const bool valid = t < T;
+        uint32_t bm[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
+        int es[MOE_MAX_TOPK];
+        for (int s = 0; s < k; ++s) {
+            int e = valid ? __ldg(idx + (size_t)t * k + s) : -1;
+            if (e >= 0 && e < E) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                    if (j == (e >> 5)) word = bm[j];
+                if (word & (1u << (e & 31))) {
+                    e = -1;  // repeat within the token: dropped
+                } else {
+#pragma unroll
+                    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                        if (j == (e >> 5)) bm[j] |= 1u << (e & 31);
+                }
+            } else {
+                e = -1;
+            }
+            es[s < MOE_MAX_TOPK ? s : 0] = e;
+        }
+        // transpose: lane b of warp w keeps M[w][32j + b]
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+            if (j < words) {
+                uint32_t mine = 0;
+#pragma unroll 4
+                for (int b = 0; b < 32; ++b) {
+                    const uint32_t m = __ballot_sync(0xffffffffu, (bm[j] >> b) & 1u);
+                    if (lane == b) mine = m;
+                }
+                s_mask[warp * ep + j * 32 + lane] = mine;
+            }
+        }
+        __syncthreads();
+        if (tid < E) {
+            int run = s_run[tid];
+            for (int w = 0; w < kBucketWarps; ++w) {
+                s_base[w * ep + tid] = run;
+                run += __popc(s_mask[w * ep + tid]);
+            }
+            s_run[tid] = run;
+        }
+        __syncthreads();
+        if (valid) {
+            const uint32_t below = (1u << lane) - 1u;
+            for (int s = 0; s < k; ++s) {
+                const int e = es[s];
+                if (e < 0) {
+                    pos[(size_t)t * k + s] = -1;
+                    continue;
+                }
+                const int p = s_off[e] + s_base[warp * ep + e] + __popc(s_mask[warp * ep + e] & below);
+                pair_tok[p] = t;
+                pair_slot[p] = s;
+                pos[(size_t)t * k + s] = p;
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0 && s_bad) flag_status(status, MOE_STATUS_BAD_INDEX);
+}
+
+}  // namespace
+
+cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok,
+                          int32_t* pair_slot, int32_t* pos, int32_t* status, cudaStream_t s) {
+    const size_t smem = (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t);
+    cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    bucket_kernel<<<1, kBucketThreads, smem, s>>>(idx, T, k, E, offsets, pair_tok, pair_slot, pos, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

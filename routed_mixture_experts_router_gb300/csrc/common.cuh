@@ -1,0 +1,89 @@
+// Shared device helpers and kernel-launcher declarations of libmoe_gb300.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over aligned groups of G lanes (G a power of two <= 32); every lane of a
+// group ends with the same value (xor butterfly: each step adds the same two
+// operands in both partner lanes).
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// 16-byte streaming load of weights: read once per kernel, so skip L1.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float ldg_half(const uint16_t* p) {
+    unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
+    return __half2float(__ushort_as_half(b));
+}
+
+// Four int8 values packed in a 32-bit word -> four exact fp32 values.
+// Each byte is biased to unsigned (xor 0x80), placed in the low mantissa byte
+// of 2^23 (0x4B0000uu = 8388608 + u), and the bias 8388608 + 128 is
+// subtracted; every step is exact.
+__device__ __forceinline__ float4 i8x4_to_f32x4(uint32_t w) {
+    const uint32_t u = w ^ 0x80808080u;
+    float4 r;
+    r.x = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
+    r.y = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
+    r.z = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
+    r.w = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
+    return r;
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+    acc = fmaf(a.z, b.z, acc);
+    acc = fmaf(a.w, b.w, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void flag_status(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---- launchers (defined in the kernel .cu files) --------------------------
+cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts, cudaStream_t s);
+
+cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok,
+                          int32_t* pair_slot, int32_t* pos, int32_t* status, cudaStream_t s);
+
+// fp32 expert path.  h: fp32 [P][d_ff] scratch.
+cudaError_t launch_ffn_f32(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
+                           const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
+                           float* out_or_ypairs, int residual, float* h, cudaStream_t s);
+
+cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
+
+cudaError_t launch_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int dm,
+                           const float* residual, float* out, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry
+point include/moe.h declares; host-side argument checks (no device work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routed_mixture_experts_router_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared():
+    src = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)
+
+
+def test_header_lists_entry_points():
+    names = declared()
+    assert sorted(names) == sorted(binding.ENTRY_POINTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert "sm_103a" in binding.version()
+
+
+def _layer(E=128, k=8, d=2048, f=768, ptr=0x10000):
+    q = binding.Q8Mat(ptr, ptr)
+    return binding.LayerW(E, k, d, f, q, q, q, ptr, 0)
+
+
+def test_workspace_size(lib):
+    w = _layer()
+    T = 1024
+    n = lib.moe_workspace_size(T, ctypes.byref(w), 0, 0)
+    P = T * 8
+    # routing (idx, wts), offsets, three pair arrays, h fp32 [P][d_ff]
+    assert n >= P * 4 * 5 + 129 * 4 + P * 768 * 4
+    assert n % 256 == 0
+    n_det = lib.moe_workspace_size(T, ctypes.byref(w), 0, binding.MOE_FLAG_DETERMINISTIC)
+    assert n_det >= n + P * 2048 * 4
+    assert lib.moe_workspace_size(T, ctypes.byref(_layer(k=0)), 0, 0) == 0
+    assert lib.moe_workspace_size(T, ctypes.byref(_layer(E=300)), 0, 0) == 0
+    assert lib.moe_workspace_size(T, ctypes.byref(_layer(d=2050)), 0, 0) == 0
+    assert lib.moe_workspace_size(-1, ctypes.byref(w), 0, 0) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(k=9, E=8), dict(k=33, E=64), dict(d=100), dict(f=0), dict(E=0)])
+def test_invalid_geometry_rejected_on_host(lib, bad):
+    w = _layer(**bad)
+    P = ctypes.c_void_p(0x10000)
+    assert lib.moe_route(P, 4, ctypes.byref(w), P, P, None) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward(P, 4, ctypes.byref(w), 0, 0, 0, ctypes.c_void_p(0x20000), None, None, None, P,
+                                 1 << 30, None, None) == binding.MOE_ERR_INVALID_ARG
+
+
+def test_invalid_pointers_rejected_on_host(lib):
+    w = _layer()
+    good = ctypes.c_void_p(0x10000)
+    mis = ctypes.c_void_p(0x10004)
+    assert lib.moe_route(mis, 4, ctypes.byref(w), good, good, None) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(None, 4, ctypes.byref(w), good, good, None) == binding.MOE_ERR_INVALID_ARG
+    # out aliasing x
+    assert lib.moe_layer_forward(good, 4, ctypes.byref(w), 0, 0, 0, good, None, None, None, good, 1 << 30, None,
+                                 None) == binding.MOE_ERR_INVALID_ARG
+    # workspace too small / misaligned
+    assert lib.moe_layer_forward(good, 4, ctypes.byref(w), 0, 0, 0, ctypes.c_void_p(0x20000), None, None, None,
+                                 good, 16, None, None) == binding.MOE_ERR_WORKSPACE
+    assert lib.moe_layer_forward(good, 4, ctypes.byref(w), 0, 0, 0, ctypes.c_void_p(0x20000), None, None, None,
+                                 ctypes.c_void_p(0x10010), 1 << 30, None, None) == binding.MOE_ERR_WORKSPACE
+    assert lib.moe_pack_q8(good, 4, 33, good, good, None) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_bucket(good, 4, 9, 8, good, good, good, good, None, None) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(good, good, good, 4, 2, 100, None, good, None) == binding.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_ok_without_device_work(lib):
+    w = _layer()
+    assert lib.moe_route(None, 0, ctypes.byref(w), None, None, None) == binding.MOE_OK
+    assert lib.moe_layer_forward(None, 0, ctypes.byref(w), 0, 0, 0, None, None, None, None, None, 0, None,
+                                 None) == binding.MOE_OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    saved = binding._lib
+    try:
+        binding._lib = None
+        with pytest.raises(RuntimeError):
+            binding.load(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved
