@@ -388,7 +388,7 @@ def run_ours(args, ws, rank, local):
             "config": workload_config(wl, args),
             "layer_hbm_gbs": layer_gbs, "near_ties": None,
             "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clocks,
+            "gpu_launches": (3 if wl.T <= 8 else 4) * args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     return 0

@@ -83,6 +83,16 @@ int check_device() {
     return cached[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
+// fp32 expert path: the streaming kernels where the geometry allows, the
+// per-expert-CTA kernels otherwise.
+cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, const int32_t* offsets, const int32_t* pair_tok,
+                       const int32_t* pair_slot, const float* wts, int fuse, float* out, int residual, float* h,
+                       int32_t* status, cudaStream_t s) {
+    if (ffn_stream_supported(w))
+        return launch_ffn_stream(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, status, s);
+    return launch_ffn_f32(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
+}
+
 inline int cuda_rc(cudaError_t e) {
     if (e == cudaSuccess) return MOE_OK;
     cudaGetLastError();
@@ -116,7 +126,7 @@ int moe_route(const float* x, int T, const moe_layer_w* w, int32_t* idx, float* 
     if (!x || !idx || !wts || !aligned16(x) || !valid_router(w)) return MOE_ERR_INVALID_ARG;
     int rc = check_device();
     if (rc) return rc;
-    return cuda_rc(launch_route(x, T, *w, idx, wts, (cudaStream_t)stream));
+    return cuda_rc(launch_route(x, T, *w, idx, wts, nullptr, nullptr, nullptr, nullptr, nullptr, (cudaStream_t)stream));
 }
 
 int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
@@ -132,7 +142,6 @@ int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_
 int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t* offsets, const int32_t* pair_tok,
                       const int32_t* pair_slot, const float* wts, int act, int fuse_combine, float* out_or_ypairs,
                       int residual, void* ws, size_t ws_bytes, int32_t* status, void* stream) {
-    (void)status;
     if (!valid_geometry(w) || !valid_T(T, w)) return MOE_ERR_INVALID_ARG;
     if (act != MOE_ACT_F32 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -146,8 +155,8 @@ int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t
     if (rc) return rc;
     if (act != MOE_ACT_F32) return MOE_ERR_UNSUPPORTED;
     char* base = static_cast<char*>(ws);
-    return cuda_rc(launch_ffn_f32(x, T, *w, offsets, pair_tok, pair_slot, wts, fuse_combine ? 1 : 0, out_or_ypairs,
-                                  residual, reinterpret_cast<float*>(base + L.h), (cudaStream_t)stream));
+    return cuda_rc(launch_ffn(x, T, *w, offsets, pair_tok, pair_slot, wts, fuse_combine ? 1 : 0, out_or_ypairs,
+                              residual, reinterpret_cast<float*>(base + L.h), status, (cudaStream_t)stream));
 }
 
 int moe_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int d_model,
@@ -185,17 +194,20 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
     int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
     float* h = reinterpret_cast<float*>(base + L.h);
-    cudaError_t e = launch_route(x, T, *w, idx, wts, s);
+    bool bucketed = false;
+    cudaError_t e = launch_route(x, T, *w, idx, wts, off, ptok, pslot, pos, &bucketed, s);
     if (e != cudaSuccess) return cuda_rc(e);
-    e = launch_bucket(idx, T, w->k, w->E, off, ptok, pslot, pos, status, s);
-    if (e != cudaSuccess) return cuda_rc(e);
+    if (!bucketed) {
+        e = launch_bucket(idx, T, w->k, w->E, off, ptok, pslot, pos, status, s);
+        if (e != cudaSuccess) return cuda_rc(e);
+    }
     if (flags & MOE_FLAG_DETERMINISTIC) {
         float* yp = reinterpret_cast<float*>(base + L.ypairs);
-        e = launch_ffn_f32(x, T, *w, off, ptok, pslot, wts, 0, yp, 0, h, s);
+        e = launch_ffn(x, T, *w, off, ptok, pslot, wts, 0, yp, 0, h, status, s);
         if (e != cudaSuccess) return cuda_rc(e);
         e = launch_combine(yp, wts, pos, T, w->k, w->d_model, residual ? x : nullptr, out, s);
     } else {
-        e = launch_ffn_f32(x, T, *w, off, ptok, pslot, wts, 1, out, residual, h, s);
+        e = launch_ffn(x, T, *w, off, ptok, pslot, wts, 1, out, residual, h, status, s);
     }
     return cuda_rc(e);
 }

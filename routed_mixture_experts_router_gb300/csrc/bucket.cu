@@ -17,6 +17,7 @@
 //      is ascending (token, slot) order within a bucket.
 // Single CTA: the work is T*k integers; latency, not bandwidth, matters.
 #include "common.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 
@@ -42,6 +43,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
     int* s_base = reinterpret_cast<int*>(bucket_dyn + kBucketWarps * ep);  // rank base of warp w in bucket e
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();  // idx written by the router
+    pdl_launch_dependents();
     if (tid < MOE_MAX_EXPERTS) {
         s_cnt[tid] = 0;
         s_run[tid] = 0;
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
 #pragma unroll
         for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
         for (int s = 0; s < k; ++s) {
-            const int e = __ldg(idx + (size_t)t * k + s);
+            const int e = __ldcg(idx + (size_t)t * k + s);
             if (e < 0 || e >= E) {
                 s_bad = 1;
                 continue;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
         for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
         int es[MOE_MAX_TOPK];
         for (int s = 0; s < k; ++s) {
-            int e = valid ? __ldg(idx + (size_t)t * k + s) : -1;
+            int e = valid ? __ldcg(idx + (size_t)t * k + s) : -1;
             if (e >= 0 && e < E) {
                 uint32_t word = 0;
 #pragma unroll
@@ -176,8 +179,17 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
     const size_t smem = (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t);
     cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    bucket_kernel<<<1, kBucketThreads, smem, s>>>(idx, T, k, E, offsets, pair_tok, pair_slot, pos, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kBucketThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bucket_kernel, idx, T, k, E, offsets, pair_tok, pair_slot, pos, status);
 }
 
 }  // namespace moe

@@ -71,7 +71,10 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
 }
 
 // ---- launchers (defined in the kernel .cu files) --------------------------
-cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts, cudaStream_t s);
+// Router (+ the bucketing too when every token fits one cluster tile and
+// `bucketed` is non-null; *bucketed then tells whether it was done).
+cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts, int32_t* offsets,
+                         int32_t* pair_tok, int32_t* pair_slot, int32_t* pos, bool* bucketed, cudaStream_t s);
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok,
                           int32_t* pair_slot, int32_t* pos, int32_t* status, cudaStream_t s);
@@ -80,6 +83,13 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
 cudaError_t launch_ffn_f32(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                            const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                            float* out_or_ypairs, int residual, float* h, cudaStream_t s);
+
+// Streaming (persistent, bulk-copy pipelined) fp32 expert path for shapes
+// with d_model, d_ff multiples of 64.
+bool ffn_stream_supported(const moe_layer_w& w);
+cudaError_t launch_ffn_stream(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
+                              const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
+                              float* out_or_ypairs, int residual, float* h, int32_t* status, cudaStream_t s);
 
 cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
 

@@ -205,7 +205,7 @@ def test_graph_replay_changed_inputs():
     case = make_case(synth.WORKLOADS["decode_t1"])
     x = case.x.clone()
     out = torch.empty_like(x)
-    ws = binding.workspace(1, case.layer)
+    ws = binding.workspace(1, case.layer, flags=binding.MOE_FLAG_DETERMINISTIC)
     binding.layer_forward(x, case.layer, out=out, ws=ws, flags=binding.MOE_FLAG_DETERMINISTIC)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
