@@ -347,7 +347,7 @@ def run_ours(args, ws, rank, local):
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": ffn_alg, "launch_ms": ffn_ms_mean,
-                "traffic": args.traffic}
+                "traffic": load_traffic("moe_expert_ffn_q8 decode") if wl.T == 1 else None}
     step_alg = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
     layer_gbs = step_alg / (ms_local / args.steps / 1e3) / 1e9
 
@@ -394,6 +394,20 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def load_traffic(key: str):
+    """DRAM bytes per launch from a committed ncu capture, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[key]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha1(src).hexdigest() != rec["source_sha1"]:
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -416,8 +430,6 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per launch of the timed kernel from an ncu capture of this build")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -23,6 +23,9 @@ SHAPES = [
     ("e8k8", 5, 256, 96, 8, 8, False),       # k == E, d_ff not a multiple of 64
     ("t2_k1", 2, 1024, 384, 64, 1, True),
     ("d4096", 9, 4096, 64, 24, 3, False),
+    ("s256_t7", 7, 256, 256, 16, 4, True),    # streaming path, all tokens staged at once
+    ("t12", 12, 1024, 512, 64, 6, True),      # streaming path, per-bucket activation chunks
+    ("t2", 2, 2048, 768, 128, 8, False),      # full geometry, two tokens
 ]
 
 
