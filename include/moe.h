@@ -180,6 +180,31 @@ MOE_API int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int a
                       int32_t* idx_out, float* wts_out, int32_t* offsets_out, void* ws, size_t ws_bytes,
                       int32_t* status, void* stream);
 
+/*
+ * moe_layer_forward without a caller workspace, for callers that cannot
+ * allocate device memory where they run the layer (a latency-critical loop
+ * that must not enter an allocator, a plugin inside a runtime that owns all
+ * device memory).  The pages have no counterpart; this is a convenience of
+ * this library.
+ *
+ * Same arguments and results as moe_layer_forward with idx_out, wts_out and
+ * offsets_out NULL; the scratch comes from one fixed region of
+ * MOE_STATIC_SCRATCH_BYTES compiled into the library (held on every GPU that
+ * loads it, until the process exits).
+ *  - Returns MOE_ERR_WORKSPACE when moe_workspace_size(T, w, act, flags)
+ *    exceeds MOE_STATIC_SCRATCH_BYTES (for the qwen3_moe geometry, T <= 64
+ *    fits with or without MOE_FLAG_DETERMINISTIC).
+ *  - Allocates nothing.  The first call on each device looks up the region's
+ *    device address (cudaGetSymbolAddress) with that device current; make it
+ *    before any stream capture.
+ *  - Every call shares the region: calls whose GPU work may overlap (other
+ *    streams, other host threads, same device) race and must be serialised
+ *    by the caller.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (8u << 20)
+MOE_API int moe_layer_forward_static(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual,
+                                     float* out, int32_t* status, void* stream);
+
 /* Library version string (static storage). */
 MOE_API const char* moe_version(void);
 

@@ -28,7 +28,8 @@ MOE_FLAG_DETERMINISTIC = 1
 _ERR = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE"}
 
 ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
-                "moe_layer_forward", "moe_version")
+                "moe_layer_forward", "moe_layer_forward_static", "moe_version")
+MOE_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -80,6 +81,8 @@ def load(path: str | None = None):
     L.moe_combine.argtypes = [P, P, P, I, I, I, P, P, P]
     L.moe_layer_forward.restype = I
     L.moe_layer_forward.argtypes = [P, I, LWP, I, I, I, P, P, P, P, P, SZ, P, P]
+    L.moe_layer_forward_static.restype = I
+    L.moe_layer_forward_static.argtypes = [P, I, LWP, I, I, I, P, P, P]
     L.moe_version.restype = ctypes.c_char_p
     L.moe_version.argtypes = []
     _lib = L
@@ -203,4 +206,16 @@ def layer_forward(x, layer: Layer, act=MOE_ACT_F32, flags=0, residual=False, out
     _check("moe_layer_forward", load().moe_layer_forward(
         _ptr(x), T, layer.ref(), act, flags, int(bool(residual)), _ptr(out), _ptr(idx_out), _ptr(wts_out),
         _ptr(offsets_out), _ptr(ws), ws.numel(), _ptr(status), _stream()))
+    return out
+
+
+def layer_forward_static(x, layer: Layer, act=MOE_ACT_F32, flags=0, residual=False, out=None, status=None):
+    """moe_layer_forward_static: the layer forward with the library's fixed
+    scratch region instead of a caller workspace (for callers that cannot
+    allocate device memory where they run the layer)."""
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, layer.d_model, dtype=torch.float32, device=x.device)
+    _check("moe_layer_forward_static", load().moe_layer_forward_static(
+        _ptr(x), T, layer.ref(), act, flags, int(bool(residual)), _ptr(out), _ptr(status), _stream()))
     return out
