@@ -16,7 +16,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-    size_t idx, wts, off, ptok, pslot, pos, h, ypairs, total;
+    size_t idx, wts, off, ptok, pslot, pos, h, xb, ypairs, total;
 };
 
 // Workspace carve-up shared by every entry point: the routing results, the
@@ -32,11 +32,12 @@ WsLayout ws_layout(int T, const moe_layer_w& w, int act, int flags) {
     L.ptok = o;   o = align_up(o + P * sizeof(int32_t));
     L.pslot = o;  o = align_up(o + P * sizeof(int32_t));
     L.pos = o;    o = align_up(o + P * sizeof(int32_t));
-    L.h = o;      o = align_up(o + P * (size_t)w.d_ff * sizeof(float));
+    L.h = o;      o = align_up(o + P * (size_t)w.d_ff * sizeof(float));   // fp32 h, or bf16 h
+    L.xb = o;                                                              // bf16 activations, bucket order
+    if (act == MOE_ACT_BF16) o = align_up(o + P * (size_t)w.d_model * sizeof(uint16_t));
     L.ypairs = o;
     if (flags & MOE_FLAG_DETERMINISTIC) o = align_up(o + P * (size_t)w.d_model * sizeof(float));
     L.total = o;
-    (void)act;
     return L;
 }
 
@@ -83,11 +84,18 @@ int check_device() {
     return cached[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
-// fp32 expert path: the streaming kernels where the geometry allows, the
-// per-expert-CTA kernels otherwise.
-cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, const int32_t* offsets, const int32_t* pair_tok,
-                       const int32_t* pair_slot, const float* wts, int fuse, float* out, int residual, float* h,
-                       int32_t* status, cudaStream_t s) {
+// Expert path: bf16 activations -> tcgen05 kernels when the batch fills at
+// least one 128-pair MMA tile (smaller batches run the fp32 path, which is
+// more accurate and memory-bound anyway); fp32 -> the streaming kernels where
+// the geometry allows, the per-expert-CTA kernels otherwise.
+cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, const int32_t* offsets,
+                       const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse, float* out,
+                       int residual, char* ws, const WsLayout& L, int32_t* status, cudaStream_t s) {
+    float* h = reinterpret_cast<float*>(ws + L.h);
+    if (act == MOE_ACT_BF16 && ffn_tc_supported(w, T))
+        return launch_ffn_tc(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual,
+                             reinterpret_cast<__nv_bfloat16*>(ws + L.xb), reinterpret_cast<__nv_bfloat16*>(h),
+                             status, s);
     if (ffn_stream_supported(w))
         return launch_ffn_stream(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, status, s);
     return launch_ffn_f32(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
@@ -153,10 +161,8 @@ int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();
     if (rc) return rc;
-    if (act != MOE_ACT_F32) return MOE_ERR_UNSUPPORTED;
-    char* base = static_cast<char*>(ws);
-    return cuda_rc(launch_ffn(x, T, *w, offsets, pair_tok, pair_slot, wts, fuse_combine ? 1 : 0, out_or_ypairs,
-                              residual, reinterpret_cast<float*>(base + L.h), status, (cudaStream_t)stream));
+    return cuda_rc(launch_ffn(x, T, *w, act, offsets, pair_tok, pair_slot, wts, fuse_combine ? 1 : 0, out_or_ypairs,
+                              residual, static_cast<char*>(ws), L, status, (cudaStream_t)stream));
 }
 
 int moe_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int d_model,
@@ -184,7 +190,6 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();
     if (rc) return rc;
-    if (act != MOE_ACT_F32) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     char* base = static_cast<char*>(ws);
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.idx);
@@ -193,7 +198,6 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     int32_t* ptok = reinterpret_cast<int32_t*>(base + L.ptok);
     int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
     int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
-    float* h = reinterpret_cast<float*>(base + L.h);
     bool bucketed = false;
     cudaError_t e = launch_route(x, T, *w, idx, wts, off, ptok, pslot, pos, &bucketed, s);
     if (e != cudaSuccess) return cuda_rc(e);
@@ -203,11 +207,11 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     }
     if (flags & MOE_FLAG_DETERMINISTIC) {
         float* yp = reinterpret_cast<float*>(base + L.ypairs);
-        e = launch_ffn(x, T, *w, off, ptok, pslot, wts, 0, yp, 0, h, status, s);
+        e = launch_ffn(x, T, *w, act, off, ptok, pslot, wts, 0, yp, 0, base, L, status, s);
         if (e != cudaSuccess) return cuda_rc(e);
         e = launch_combine(yp, wts, pos, T, w->k, w->d_model, residual ? x : nullptr, out, s);
     } else {
-        e = launch_ffn(x, T, *w, off, ptok, pslot, wts, 1, out, residual, h, status, s);
+        e = launch_ffn(x, T, *w, act, off, ptok, pslot, wts, 1, out, residual, base, L, status, s);
     }
     return cuda_rc(e);
 }

@@ -91,6 +91,13 @@ cudaError_t launch_ffn_stream(const float* x, int T, const moe_layer_w& w, const
                               const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                               float* out_or_ypairs, int residual, float* h, int32_t* status, cudaStream_t s);
 
+// Tensor-core (tcgen05) bf16 expert path for prefill-size batches.
+bool ffn_tc_supported(const moe_layer_w& w, int T);
+cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
+                          const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
+                          float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
+                          cudaStream_t s);
+
 cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
 
 cudaError_t launch_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int dm,

@@ -1,0 +1,588 @@
+// Expert SwiGLU FFNs on the tcgen05 tensor cores (the prefill path): bf16
+// operands, fp32 accumulation in TMEM, Q8_0 dequantisation fused into the
+// operand staging, SwiGLU fused into the gate/up epilogue and the weighted
+// combine fused into the down epilogue.
+//
+//   gather   xb[p] = bf16(x[token(p)])                      pairs in bucket order
+//   gate/up  h[p][r] = bf16( silu(Wg_e[r] . xb[p]) * (Wu_e[r] . xb[p]) )
+//   down     out[t][o] += w[t][slot] * (Wd_e[o] . h[p])     (or ypairs[p][o])
+// Q8_0 weights w = q * d (amalgafy.com/technical-overview, "Validated GPU
+// foundation"); down projection K=768 -> 2048 rows and prefill batches of
+// 768 / 1024 tokens (expxa.com reuse-ordering-qualification, "What changed
+// from the first experiment"); activations cast for the expert contraction
+// ("including routing and quantization", same page, "Operator gains ...").
+//
+// Design (one persistent 512-thread CTA per SM).  A work unit is one expert,
+// one 128-row tile of its weight matrix (the MMA M dimension: "swap AB", so
+// the small, ragged token count is N) and up to 128 of its tokens (N, padded
+// to a multiple of 16).  Warp roles:
+//   warp 0       TMA producer: int8 weight tiles (128 rows x 128 K, 128-byte
+//                swizzle) into a raw ring; bf16 token tiles (N x 64 K) into
+//                the operand ring
+//   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, M=128,
+//                K=16 per instruction, into a double-buffered TMEM accumulator
+//   warps 4-11   dequantisation: thread = (row, half of K); int8 -> fp32
+//                exactly, times the block's fp16 scale, -> bf16 (RNE), written
+//                in the 128-byte-swizzled K-major layout the MMA reads
+//   warps 12-15  epilogue: tcgen05.ld of the accumulator (TMEM lane = row),
+//                SwiGLU -> bf16 h, or the weighted combine into out
+// Every mbarrier wait is bounded: past the deadline the CTA flags
+// MOE_STATUS_TIMEOUT in the status word and stops; all copies and MMAs it
+// started are drained before TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "pipeline.cuh"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTcThreads = 512;
+constexpr int kBM = 128;      // weight rows per unit (MMA M)
+constexpr int kBKR = 128;     // int8 K per raw stage (one 128-byte row)
+constexpr int kBK = 64;       // bf16 K per operand stage (one 128-byte row)
+constexpr int kBN = 128;      // max tokens per unit (MMA N)
+constexpr int kBRows = 32;    // token rows per TMA box
+constexpr int kRS = 2;        // raw ring stages
+constexpr int kTile = 16384;  // one 128 x 128-byte tile
+constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12;
+
+struct TcParams {
+    int K;     // reduction length (d_model for gate/up, d_ff for down)
+    int rows;  // weight rows per expert (d_ff for gate/up, d_model for down)
+    int E, T, k;
+    const int32_t* offsets;
+    const int32_t* pair_tok;
+    const int32_t* pair_slot;
+    const float* wts;
+    const uint16_t* d0;  // fp16 scales of matrix 0 (gate or down)
+    const uint16_t* d1;  // fp16 scales of matrix 1 (up) or null
+    __nv_bfloat16* h;    // EPI 0: h [P][rows]
+    float* out;          // EPI 1: out [T][rows] (+=); EPI 2: ypairs [P][rows]
+    int32_t* status;
+};
+
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// two fp32 -> bf16x2 (round to nearest even); `lo` lands in the low half
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16 int8 (one 16-byte word) times scale d -> 16 bf16 (two 16-byte words).
+__device__ __forceinline__ void dequant16(uint4 q, float d, uint4& o0, uint4& o1) {
+    const f32x2 bias = 0xCB000080CB000080ull;  // (-(2^23 + 128), -(2^23 + 128))
+    const f32x2 dd = f2_pack(d, d);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t r[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t u = w[m] ^ 0x80808080u;
+        f32x2 lo = f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
+        f32x2 hi = f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
+        lo = f2_mul(f2_add(lo, bias), dd);  // q exact, q*d exact in fp32
+        hi = f2_mul(f2_add(hi, bias), dd);
+        float a, b, c, e;
+        f2_unpack(lo, a, b);
+        f2_unpack(hi, c, e);
+        r[2 * m] = bf16x2_rn(a, b);
+        r[2 * m + 1] = bf16x2_rn(c, e);
+    }
+    o0 = make_uint4(r[0], r[1], r[2], r[3]);
+    o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Active experts in id order (warp-wide); buckets cut into chunks of kBN pairs.
+__device__ void tc_build_active(const int32_t* offsets, int E, int* s_act, int* s_beg, int* s_end, int* s_cb,
+                                int* s_n) {
+    const int lane = threadIdx.x & 31;
+    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+        const int e = 32 * j + lane;
+        lo[j] = e < E ? __ldcg(offsets + e) : 0;
+        hi[j] = e < E ? __ldcg(offsets + e + 1) : 0;
+    }
+    int n = 0, nc = 0;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+        const bool a = hi[j] > lo[j];
+        const uint32_t m = __ballot_sync(0xffffffffu, a);
+        const int my_c = a ? (hi[j] - lo[j] + kBN - 1) / kBN : 0;
+        int incl = my_c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (a) {
+            const int jj = n + __popc(m & ((1u << lane) - 1u));
+            s_act[jj] = 32 * j + lane;
+            s_beg[jj] = lo[j];
+            s_end[jj] = hi[j];
+            s_cb[jj] = nc + incl - my_c;
+        }
+        n += __popc(m);
+        nc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        *s_n = n;
+        s_cb[n] = nc;
+    }
+}
+
+struct Unit {
+    int e, m0, p0, nv, N;  // expert, first weight row, first pair, valid pairs, MMA N
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int mt, const int* s_act, const int* s_beg, const int* s_end,
+                                            const int* s_cb, int n) {
+    const int g = u / mt;
+    Unit U;
+    U.m0 = (u - g * mt) * kBM;
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_cb[mid] <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    U.e = s_act[lo];
+    U.p0 = s_beg[lo] + (g - s_cb[lo]) * kBN;
+    U.nv = min(kBN, s_end[lo] - U.p0);
+    U.N = (U.nv + 15) & ~15;
+    return U;
+}
+
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort_flag) {
+    if (mbar_wait(bar, parity)) return true;
+    flag_status(status, MOE_STATUS_TIMEOUT_BIT);
+    *abort_flag = 1;
+    return false;
+}
+
+template <int NMAT, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_ffn_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                  const __grid_constant__ CUtensorMap tm_b, TcParams p) {
+    constexpr int AS = NMAT == 2 ? 3 : 4;  // operand ring stages
+    constexpr uint32_t kTmemCols = NMAT * kBN * 2;
+    extern __shared__ unsigned char tc_smem_raw[];
+    __shared__ __align__(8) uint64_t raw_full[kRS], raw_empty[kRS], b_full[AS], a_full[AS], ab_empty[AS];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain_bar;
+    __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
+    __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ int s_ep_tok[kBN];
+    __shared__ float s_ep_w[kBN];
+
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char* raw = smem;                                   // [kRS][NMAT][kTile]
+    unsigned char* As = raw + kRS * NMAT * kTile;                // [AS][NMAT][kTile]
+    unsigned char* Bs = As + AS * NMAT * kTile;                  // [AS][kTile]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRS; ++s) {
+            mbar_init(raw_full + s, 1);
+            mbar_init(raw_empty + s, kDqWarps);
+        }
+        for (int s = 0; s < AS; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(a_full + s, kDqWarps);
+            mbar_init(ab_empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 4);
+        }
+        mbar_init(&drain_bar, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_a0);
+        if (NMAT == 2) prefetch_tmap(&tm_a1);
+        prefetch_tmap(&tm_b);
+    }
+    pdl_wait();  // bucketing and the previous stage's activations are complete
+    if (warp == 2) tc_build_active(p.offsets, p.E, s_act, s_beg, s_end, s_cb, &s_n);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_launch_dependents();
+    const uint32_t tmem = s_tmem;
+    const int mt = p.rows / kBM;
+    const int n_units = s_cb[s_n] * mt;
+    const int kr_n = p.K / kBKR;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            uint32_t rc = 0, ac = 0;
+            for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const int wrow = U.e * p.rows + U.m0;
+                const int nb = (U.N + kBRows - 1) / kBRows;
+                for (int kr = 0; kr < kr_n; ++kr) {
+                    const int rs = rc % kRS;
+                    if (!tc_wait(raw_empty + rs, ((rc / kRS) & 1) ^ 1, p.status, &s_abort)) break;
+                    mbar_arrive_expect_tx(raw_full + rs, NMAT * kTile);
+                    tma_load_2d_hint(raw + (rs * NMAT + 0) * kTile, &tm_a0, kr * kBKR, wrow, raw_full + rs, pol);
+                    if (NMAT == 2)
+                        tma_load_2d_hint(raw + (rs * NMAT + 1) * kTile, &tm_a1, kr * kBKR, wrow, raw_full + rs, pol);
+                    ++rc;
+                    for (int j = 0; j < 2; ++j) {
+                        const int s = ac % AS;
+                        if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
+                        mbar_arrive_expect_tx(b_full + s, nb * kBRows * 128);
+                        for (int bb = 0; bb < nb; ++bb)
+                            tma_load_2d(Bs + s * kTile + bb * kBRows * 128, &tm_b, kr * kBKR + j * kBK,
+                                        U.p0 + bb * kBRows, b_full + s);
+                        ++ac;
+                    }
+                    if (s_abort) break;
+                }
+            }
+            // drain: every issued copy has landed before the CTA can exit
+            for (uint32_t c = (rc > kRS ? rc - kRS : 0); c < rc; ++c) mbar_wait(raw_full + c % kRS, (c / kRS) & 1);
+            for (uint32_t c = (ac > AS ? ac - AS : 0); c < ac; ++c) mbar_wait(b_full + c % AS, (c / AS) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t ac = 0, uc = 0;
+            for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const int buf = uc & 1;
+                if (!tc_wait(acc_empty + buf, ((uc >> 1) & 1) ^ 1, p.status, &s_abort)) break;
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_bf16(kBM, U.N);
+                const uint32_t dcol = tmem + buf * NMAT * kBN;
+                for (int ks = 0; ks < p.K / kBK; ++ks) {
+                    const int s = ac % AS;
+                    if (!tc_wait(a_full + s, (ac / AS) & 1, p.status, &s_abort)) break;
+                    if (!tc_wait(b_full + s, (ac / AS) & 1, p.status, &s_abort)) break;
+                    tc_fence_after();
+                    const uint64_t bdesc = umma_desc_sw128(Bs + s * kTile);
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+                        const uint64_t adesc = umma_desc_sw128(As + (s * NMAT + mat) * kTile);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
+                            umma_bf16(dcol + mat * kBN, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+                    }
+                    umma_commit(ab_empty + s);
+                    ++ac;
+                }
+                if (s_abort) break;
+                umma_commit(acc_full + buf);
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            umma_commit(&drain_bar);
+            mbar_wait(&drain_bar, 0);
+        }
+    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+        // ---------------------------------------------------------------- dequantisation
+        const int tq = (warp - kDqWarp0) * 32 + lane;
+        const int r = tq & (kBM - 1), hf = tq >> 7;  // row, half of each 64-K operand stage
+        const int nbk = p.K / 32;                    // scale blocks per row
+        uint32_t rc = 0, ac = 0;
+        for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
+            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+            const size_t srow = (size_t)(U.e * p.rows + U.m0 + r) * nbk;
+            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1
+            float dc[NMAT][2], dn[NMAT][2];
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat) {
+                const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) dc[mat][j] = ldg_half(dp + srow + 2 * j + hf);
+            }
+            for (int kr = 0; kr < kr_n; ++kr) {
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat) {
+                    const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        dn[mat][j] = (kr + 1 < kr_n) ? ldg_half(dp + srow + 4 * (kr + 1) + 2 * j + hf) : 0.f;
+                }
+                const int rs = rc % kRS;
+                if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) break;
+                for (int j = 0; j < 2; ++j) {
+                    const int s = ac % AS;
+                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+                        const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
+                        unsigned char* at = As + (s * NMAT + mat) * kTile;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + 2 * hf + i));
+                            uint4 o0, o1;
+                            dequant16(q, dc[mat][j], o0, o1);
+                            *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i)) = o0;
+                            *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i + 1)) = o1;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_full + s);
+                    ++ac;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(raw_empty + rs);
+                ++rc;
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat) {
+                    dc[mat][0] = dn[mat][0];
+                    dc[mat][1] = dn[mat][1];
+                }
+                if (s_abort) break;
+            }
+        }
+    } else if (warp >= kEpWarp0) {
+        // ---------------------------------------------------------------- epilogue
+        const int ew = warp - kEpWarp0;   // == warp % 4: TMEM lanes 32*ew .. 32*ew+31
+        const int row = ew * 32 + lane;   // weight row within the unit
+        const int et = ew * 32 + lane;    // pair slot staged by this thread
+        uint32_t uc = 0;
+        for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
+            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+            if (EPI == 1) {
+                int tok = -1;
+                float w = 0.f;
+                if (et < U.nv) {
+                    const int pp = U.p0 + et;
+                    const int t = __ldcg(p.pair_tok + pp), sl = __ldcg(p.pair_slot + pp);
+                    if (t >= 0 && t < p.T && sl >= 0 && sl < p.k) {
+                        tok = t;
+                        w = __ldcg(p.wts + (size_t)t * p.k + sl);
+                    }
+                }
+                s_ep_tok[et] = tok;
+                s_ep_w[et] = w;
+                named_bar(2, 128);
+            }
+            const int buf = uc & 1;
+            if (!tc_wait(acc_full + buf, (uc >> 1) & 1, p.status, &s_abort)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + buf * NMAT * kBN;
+            for (int c0 = 0; c0 < U.N; c0 += 16) {
+                float g[16], v[16];
+                tmem_ld16(tbase + c0, g);
+                if (NMAT == 2) tmem_ld16(tbase + kBN + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int n = c0 + i;
+                    if (n < U.nv) {
+                        const size_t pp = (size_t)(U.p0 + n);
+                        if (EPI == 0) {
+                            p.h[pp * p.rows + U.m0 + row] = __float2bfloat16_rn(silu_f(g[i]) * v[i]);
+                        } else if (EPI == 1) {
+                            const int tok = s_ep_tok[n];
+                            if (tok >= 0) atomicAdd(p.out + (size_t)tok * p.rows + U.m0 + row, s_ep_w[n] * g[i]);
+                        } else {
+                            p.out[pp * p.rows + U.m0 + row] = g[i];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            named_bar(2, 128);  // every epilogue thread is done with this buffer and the staged pairs
+            if (lane == 0) mbar_arrive(acc_empty + buf);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// x (fp32, token order) -> xb (bf16, bucket order); also the combine target
+// out = residual ? x : 0 for the down kernel's atomics.
+__global__ void gather_bf16_kernel(const float* __restrict__ x, int T, int dm, const int32_t* __restrict__ pair_tok,
+                                   const int32_t* __restrict__ offsets, int E, int P, __nv_bfloat16* __restrict__ xb,
+                                   float* __restrict__ out_init, int residual) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int pv = __ldcg(offsets + E);
+    const int c8 = dm / 8;
+    const size_t n = (size_t)P * c8;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int pp = (int)(i / c8), c = (int)(i - (size_t)pp * c8);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        const int t = pp < pv ? __ldcg(pair_tok + pp) : -1;
+        if (t >= 0 && t < T) {
+            const float4* src = reinterpret_cast<const float4*>(x + (size_t)t * dm) + 2 * c;
+            const float4 a = __ldcg(src), b = __ldcg(src + 1);
+            o.x = bf16x2_rn(a.x, a.y);
+            o.y = bf16x2_rn(a.z, a.w);
+            o.z = bf16x2_rn(b.x, b.y);
+            o.w = bf16x2_rn(b.z, b.w);
+        }
+        reinterpret_cast<uint4*>(xb)[i] = o;
+    }
+    if (out_init) {
+        const size_t n4 = (size_t)T * dm / 4;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+            reinterpret_cast<float4*>(out_init)[i] =
+                residual ? __ldcg(reinterpret_cast<const float4*>(x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D K-major map: inner dimension K (elements), outer `rows`, box {bx, by}, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K, uint64_t rows,
+               uint32_t bx, uint32_t by) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * (uint64_t)esize};
+    const cuuint32_t box[2] = {bx, by};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_num_sms() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+template <int NMAT, int EPI>
+cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const TcParams& p,
+                      cudaStream_t s) {
+    constexpr int AS = NMAT == 2 ? 3 : 4;
+    const size_t smem = (size_t)(kRS * NMAT + AS * NMAT + AS) * kTile + 1024;
+    auto kern = tc_ffn_kernel<NMAT, EPI>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tc_num_sms(), 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a0, a1, b, p);
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_layer_w& w, int T) {
+    return w.d_model % kBKR == 0 && w.d_ff % kBKR == 0 && w.d_model % kBM == 0 && w.d_ff % kBM == 0 &&
+           (long long)T * w.k >= kBN && encode_fn() != nullptr;
+}
+
+cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
+                          const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
+                          float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
+                          cudaStream_t s) {
+    const int P = T * w.k;
+    const int dm = w.d_model, f = w.d_ff;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(tc_num_sms() * 4, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t err = cudaLaunchKernelEx(&cfg, gather_bf16_kernel, x, T, dm, pair_tok, offsets, w.E, P, xb,
+                                             fuse_combine ? out_or_ypairs : (float*)nullptr, residual);
+        if (err != cudaSuccess) return err;
+    }
+    CUtensorMap tg, tu, td, txb, th;
+    if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, (uint64_t)w.E * f, kBKR, kBM) ||
+        !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, (uint64_t)w.E * f, kBKR, kBM) ||
+        !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, (uint64_t)w.E * dm, kBKR, kBM) ||
+        !make_tmap(&txb, xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dm, P, kBK, kBRows) ||
+        !make_tmap(&th, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, P, kBK, kBRows))
+        return cudaErrorInvalidValue;
+    TcParams pg = {};
+    pg.K = dm;
+    pg.rows = f;
+    pg.E = w.E;
+    pg.T = T;
+    pg.k = w.k;
+    pg.offsets = offsets;
+    pg.pair_tok = pair_tok;
+    pg.pair_slot = pair_slot;
+    pg.wts = wts;
+    pg.d0 = w.gate.d;
+    pg.d1 = w.up.d;
+    pg.h = hb;
+    pg.status = status;
+    cudaError_t err = launch_tc<2, 0>(tg, tu, txb, pg, s);
+    if (err != cudaSuccess) return err;
+    TcParams pd = pg;
+    pd.K = f;
+    pd.rows = dm;
+    pd.d0 = w.down.d;
+    pd.d1 = nullptr;
+    pd.h = nullptr;
+    pd.out = out_or_ypairs;
+    if (fuse_combine) return launch_tc<1, 1>(td, td, th, pd, s);
+    return launch_tc<1, 2>(td, td, th, pd, s);
+}
+
+}  // namespace moe
