@@ -16,7 +16,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-    size_t idx, wts, off, ptok, pslot, pos, h, xb, ypairs, total;
+    size_t idx, wts, off, ptok, pslot, pos, h, xb, ypairs, lg, sync, total;
 };
 
 // Workspace carve-up shared by every entry point: the routing results, the
@@ -37,6 +37,8 @@ WsLayout ws_layout(int T, const moe_layer_w& w, int act, int flags) {
     if (act == MOE_ACT_BF16) o = align_up(o + P * (size_t)w.d_model * sizeof(uint16_t));
     L.ypairs = o;
     if (flags & MOE_FLAG_DETERMINISTIC) o = align_up(o + P * (size_t)w.d_model * sizeof(float));
+    L.lg = o;     o = align_up(o + (size_t)T * w.E * sizeof(float));         // router logits (fused decode)
+    L.sync = o;   o = align_up(o + 2 * sizeof(unsigned int));               // grid-barrier words (fused decode)
     L.total = o;
     return L;
 }
@@ -198,6 +200,19 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     int32_t* ptok = reinterpret_cast<int32_t*>(base + L.ptok);
     int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
     int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
+    // One or two decode tokens on the fp32 path: the whole layer in one
+    // cooperative launch (falls through to the separate kernels if the device
+    // cannot co-schedule it).
+    const bool f32_path = act == MOE_ACT_F32 || !ffn_tc_supported(*w, T);
+    if (f32_path && !(flags & MOE_FLAG_DETERMINISTIC) && decode_fused_supported(*w, T)) {
+        const cudaError_t fe = launch_decode_fused(x, T, *w, residual, out, idx_out, wts_out, offsets_out,
+                                                   reinterpret_cast<float*>(base + L.lg),
+                                                   reinterpret_cast<float*>(base + L.h),
+                                                   reinterpret_cast<unsigned int*>(base + L.sync), status, s);
+        if (fe == cudaSuccess) return MOE_OK;
+        if (fe != cudaErrorCooperativeLaunchTooLarge && fe != cudaErrorInvalidConfiguration) return cuda_rc(fe);
+        cudaGetLastError();
+    }
     bool bucketed = false;
     cudaError_t e = launch_route(x, T, *w, idx, wts, off, ptok, pslot, pos, &bucketed, s);
     if (e != cudaSuccess) return cuda_rc(e);

@@ -58,8 +58,13 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
         uint32_t bm[MOE_MAX_EXPERTS / 32];
 #pragma unroll
         for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
-        for (int s = 0; s < k; ++s) {
-            const int e = __ldcg(idx + (size_t)t * k + s);
+        int ids[MOE_MAX_TOPK];  // all of the token's ids in one round trip
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) ids[s] = s < k ? __ldcg(idx + (size_t)t * k + s) : -1;
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) {
+            if (s >= k) break;
+            const int e = ids[s];
             if (e < 0 || e >= E) {
                 s_bad = 1;
                 continue;
@@ -111,8 +116,12 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
 #pragma unroll
         for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
         int es[MOE_MAX_TOPK];
-        for (int s = 0; s < k; ++s) {
-            int e = valid ? __ldcg(idx + (size_t)t * k + s) : -1;
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) es[s] = (valid && s < k) ? __ldcg(idx + (size_t)t * k + s) : -1;
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) {
+            if (s >= k) break;
+            int e = es[s];
             if (e >= 0 && e < E) {
                 uint32_t word = 0;
 #pragma unroll
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
             } else {
                 e = -1;
             }
-            es[s < MOE_MAX_TOPK ? s : 0] = e;
+            es[s] = e;
         }
         // transpose: lane b of warp w keeps M[w][32j + b]
 #pragma unroll
@@ -155,7 +164,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
         __syncthreads();
         if (valid) {
             const uint32_t below = (1u << lane) - 1u;
-            for (int s = 0; s < k; ++s) {
+#pragma unroll
+            for (int s = 0; s < MOE_MAX_TOPK; ++s) {
+                if (s >= k) break;
                 const int e = es[s];
                 if (e < 0) {
                     pos[(size_t)t * k + s] = -1;

@@ -98,6 +98,13 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
                           float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
                           cudaStream_t s);
 
+// The whole layer for T <= 2 decode tokens in one cooperative launch (fp32
+// path).  logits: [T][E] scratch; h: [T*k][d_ff] scratch; sync: 2 words.
+bool decode_fused_supported(const moe_layer_w& w, int T);
+cudaError_t launch_decode_fused(const float* x, int T, const moe_layer_w& w, int residual, float* out,
+                                int32_t* idx_out, float* wts_out, int32_t* offsets_out, float* logits, float* h,
+                                unsigned int* sync, int32_t* status, cudaStream_t s);
+
 cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
 
 cudaError_t launch_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int dm,

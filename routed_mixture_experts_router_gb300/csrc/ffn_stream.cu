@@ -26,164 +26,13 @@
 // streaming Wd before gate/up finishes and waits only before reading h.
 #include "common.cuh"
 #include "pipeline.cuh"
+#include "stream_common.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kMaxStagedPairs = 256;  // pair metadata staged in shared memory
-constexpr int kDnRowsPerItem = 4;     // down item: 4 rows, 2 per half-warp
-
-typedef unsigned long long f32x2;
-
-__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
-    f32x2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float f2_sum(f32x2 v) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-    return a + b;
-}
-__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
-    f32x2 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
-    f32x2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-// One word of four int8 -> (q0, q1), (q2, q3) as exact fp32 pairs.
-__device__ __forceinline__ void i8x4_to_f2(uint32_t w, f32x2& lo, f32x2& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const f32x2 bias = 0xCB000080CB000080ull;  // (-(2^23 + 128), -(2^23 + 128))
-    lo = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                        __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
-                bias);
-    hi = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                        __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
-                bias);
-}
-
-// sum over 16 values of q * x: one 16-byte weight chunk, four float4 of x at stride `st`.
-__device__ __forceinline__ float chunk_dot(const uint4 q, const float4* xv4, int st) {
-    f32x2 acc = 0ull;
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        f32x2 lo, hi;
-        i8x4_to_f2(w[m], lo, hi);
-        const float4 xv = xv4[m * st];
-        acc = f2_fma(lo, f2_pack(xv.x, xv.y), acc);
-        acc = f2_fma(hi, f2_pack(xv.z, xv.w), acc);
-    }
-    return f2_sum(acc);
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Shared-memory layout of one staged activation vector for LPR lanes that
-// split K in 16-value chunks c = hl + LPR*m: float4 j of chunk c sits at
-// (m*4 + j)*LPR + hl, so one load instruction reads consecutive float4s.
-template <int LPR>
-__device__ __forceinline__ int stage_idx(int q) {
-    const int c = q >> 2, j = q & 3;
-    return ((c / LPR) * 4 + j) * LPR + (c % LPR);
-}
-
-// Active experts (non-empty buckets) in id order, by warp 0, and the work
-// list they imply: expert a's bucket is cut into chunks of at most `chunk`
-// pairs (the activations one pass stages in shared memory); s_cb[a] is the
-// index of a's first chunk and s_cb[n] the total.  All offsets are fetched in
-// one round trip, through L2 (they were written by an earlier kernel).
-__device__ void build_active(const int32_t* offsets, int E, int chunk, int* s_act, int* s_beg, int* s_end,
-                             int* s_cb, int* s_n) {
-    const int lane = threadIdx.x & 31;
-    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
-        const int e = 32 * j + lane;
-        lo[j] = e < E ? __ldcg(offsets + e) : 0;
-        hi[j] = e < E ? __ldcg(offsets + e + 1) : 0;
-    }
-    int n = 0, nc = 0;
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
-        const bool a = hi[j] > lo[j];
-        const uint32_t m = __ballot_sync(0xffffffffu, a);
-        const int my_c = a ? (hi[j] - lo[j] + chunk - 1) / chunk : 0;
-        int incl = my_c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (a) {
-            const int jj = n + __popc(m & ((1u << lane) - 1u));
-            s_act[jj] = 32 * j + lane;
-            s_beg[jj] = lo[j];
-            s_end[jj] = hi[j];
-            s_cb[jj] = nc + incl - my_c;
-        }
-        n += __popc(m);
-        nc += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-        *s_n = n;
-        s_cb[n] = nc;
-    }
-}
-
-// Global chunk g -> active expert index a (largest a with s_cb[a] <= g).
-__device__ __forceinline__ int locate(int g, const int* s_cb, int n) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_cb[mid] <= g) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ void item_range(int n_items, int* lo, int* hi) {
-    const long long b = blockIdx.x, G = gridDim.x;
-    *lo = (int)(b * n_items / G);
-    *hi = (int)((b + 1) * n_items / G);
-}
-
-// A warp walks items lo + warp, lo + warp + NW, ... of [lo, hi) that share a
-// segment (same bucket chunk).  issue(i, stage) starts the copies of item i
-// and commits them; compute(i, stage) runs once they have landed.  NSTG - 1
-// items are always in flight ahead of the one being computed.
-template <int NSTG, typename Issue, typename Compute>
-__device__ __forceinline__ void warp_stream(int first, int end, int step, Issue issue, Compute compute) {
-    int n = first < end ? (end - first + step - 1) / step : 0;
-#pragma unroll
-    for (int j = 0; j < NSTG - 1; ++j) {
-        if (j < n) issue(first + j * step, j);
-        else cp_async_commit();
-    }
-    for (int j = 0; j < n; ++j) {
-        const int jn = j + NSTG - 1;
-        if (jn < n) issue(first + jn * step, jn % NSTG);
-        else cp_async_commit();
-        cp_async_wait<NSTG - 1>();
-        __syncwarp();
-        compute(first + j * step, j % NSTG);
-        __syncwarp();  // every lane done with this stage before it is refilled
-    }
-}
+using namespace stream;
 
 // ============================================================== gate / up ==
 // One warp per output feature r (its gate row and up row); lanes split
@@ -200,10 +49,11 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
     __shared__ int s_tok[ALLTOK ? kMaxStagedPairs : 1];
+    __shared__ int s_segtok[ALLTOK ? 1 : kMaxStagedPairs];
     constexpr int kThreads = NW * 32;
     constexpr int kTok4 = KCH * 4 * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d4 = dm / 4, nch = dm / 16;
+    const int d4 = dm / 4;
     const int item_bytes = 2 * dm + 2 * (dm / 16);  // gate qs, up qs, gate d, up d
     unsigned char* ring = gu_smem + (size_t)warp * NSTG * item_bytes;
     float4* xs = reinterpret_cast<float4*>(gu_smem + (size_t)NW * NSTG * item_bytes);
@@ -235,22 +85,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
     // item i = (global chunk i / f, feature i % f)
     auto issue = [&](int i, int st) {
         const int g = i / f, r = i - g * f;
-        const size_t row = (size_t)s_act[locate(g, s_cb, s_n)] * f + r;
-        unsigned char* b = ring + (size_t)st * item_bytes;
-#pragma unroll
-        for (int m = 0; m < KCH; ++m) {
-            const int c = lane + 32 * m;
-            if (c < nch) {
-                cp_async16(b + c * 16, gqs + row * dm + c * 16);
-                cp_async16(b + dm + c * 16, uqs + row * dm + c * 16);
-            }
-        }
-        const int sp = dm / 256;  // 16-byte pieces of one row's scales
-        if (lane < sp) cp_async16(b + 2 * dm + lane * 16, reinterpret_cast<const unsigned char*>(gd) + row * (dm / 16) + lane * 16);
-        else if (lane < 2 * sp)
-            cp_async16(b + 2 * dm + dm / 16 + (lane - sp) * 16,
-                       reinterpret_cast<const unsigned char*>(ud) + row * (dm / 16) + (lane - sp) * 16);
-        cp_async_commit();
+        gu_issue_item<KCH>(ring + (size_t)st * item_bytes, gqs, uqs, gd, ud,
+                           (size_t)s_act[locate(g, s_cb, s_n)] * f + r, dm, lane);
     };
     auto compute = [&](int i, int st) {
         const int g = i / f, r = i - g * f;
@@ -258,47 +94,10 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
         const int c0 = g - s_cb[a];
         const int pb = ALLTOK ? s_beg[a] : s_beg[a] + c0 * tca;
         const int pe = ALLTOK ? s_end[a] : min(s_end[a], pb + tca);
-        const unsigned char* b = ring + (size_t)st * item_bytes;
-        const __half* gsc = reinterpret_cast<const __half*>(b + 2 * dm);
-        const __half* usc = reinterpret_cast<const __half*>(b + 2 * dm + dm / 16);
-        for (int pp = pb; pp < pe; pp += G) {
-            const int ng = min(G, pe - pp);
-            int toff[G];
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2)
-                toff[g2] = (g2 < ng ? (ALLTOK ? s_tok[pp + g2] : (pp + g2 - pb)) : 0) * kTok4;
-            float ga[G], ua[G];
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2) {
-                ga[g2] = 0.f;
-                ua[g2] = 0.f;
-            }
-#pragma unroll
-            for (int m = 0; m < KCH; ++m) {
-                const int c = lane + 32 * m;
-                if (c < nch) {
-                    const uint4 qg = *reinterpret_cast<const uint4*>(b + c * 16);
-                    const uint4 qu = *reinterpret_cast<const uint4*>(b + dm + c * 16);
-                    const float sg = __half2float(gsc[c >> 1]), su = __half2float(usc[c >> 1]);
-#pragma unroll
-                    for (int g2 = 0; g2 < G; ++g2) {
-                        if (g2 < ng) {
-                            const float4* xv = xs + toff[g2] + m * 4 * 32 + lane;
-                            ga[g2] = fmaf(sg, chunk_dot(qg, xv, 32), ga[g2]);
-                            ua[g2] = fmaf(su, chunk_dot(qu, xv, 32), ua[g2]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2) {
-                ga[g2] = warp_sum(ga[g2]);
-                ua[g2] = warp_sum(ua[g2]);
-            }
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2)
-                if (lane == g2 && g2 < ng) h[(size_t)(pp + g2) * f + r] = silu_f(ga[g2]) * ua[g2];
-        }
+        if constexpr (G == kMultiG)
+            gu_compute_multi<KCH, ALLTOK>(ring + (size_t)st * item_bytes, r, pb, pe, dm, f, lane, xs, s_tok, h);
+        else
+            gu_compute_item<KCH, G, ALLTOK>(ring + (size_t)st * item_bytes, r, pb, pe, dm, f, lane, xs, s_tok, h);
     };
 
     if (ALLTOK) {
@@ -311,9 +110,12 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
             const int pb = s_beg[a] + (g - s_cb[a]) * tca;
             const int pe = min(s_end[a], pb + tca);
             __syncthreads();  // the previous segment's activations are no longer read
+            for (int j = threadIdx.x; j < pe - pb; j += kThreads) s_segtok[j] = __ldcg(pair_tok + pb + j);
+            __syncthreads();
+#pragma unroll 4
             for (int q = threadIdx.x; q < (pe - pb) * d4; q += kThreads) {
                 const int jj = q / d4, qq = q - jj * d4;
-                const int t = __ldcg(pair_tok + pb + jj);
+                const int t = s_segtok[jj];
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (t >= 0 && t < T) v = __ldcg(reinterpret_cast<const float4*>(x) + (size_t)t * d4 + qq);
                 xs[jj * kTok4 + stage_idx<32>(qq)] = v;
@@ -341,12 +143,14 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
     __shared__ int s_ptok[ALLP ? kMaxStagedPairs : 1];
     __shared__ float s_pw[ALLP ? kMaxStagedPairs : 1];
+    __shared__ int s_segtok[ALLP ? 1 : kMaxStagedPairs];
+    __shared__ float s_segw[ALLP ? 1 : kMaxStagedPairs];
     constexpr int kThreads = NW * 32;
     constexpr int LPR = 16;
     constexpr int kTok4 = KCH * 4 * LPR;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hl = lane & 15, sub = lane >> 4;
-    const int f4 = f / 4, nch = f / 16;
+    const int f4 = f / 4;
     const int P = T * k;
     const int nq = dm / kDnRowsPerItem;
     const int item_bytes = kDnRowsPerItem * f + kDnRowsPerItem * (f / 16);  // qs rows, then their scales
@@ -362,15 +166,8 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
 
     auto issue = [&](int i, int st) {
         const int g = i / nq, qd = i - g * nq;
-        const size_t row0 = (size_t)s_act[locate(g, s_cb, s_n)] * dm + (size_t)qd * kDnRowsPerItem;
-        unsigned char* b = ring + (size_t)st * item_bytes;
-        const int qpieces = kDnRowsPerItem * f / 16;  // contiguous qs of the 4 rows
-        const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(dqs) + row0 * f;
-        for (int pc = lane; pc < qpieces; pc += 32) cp_async16(b + pc * 16, qsrc + pc * 16);
-        const int spieces = kDnRowsPerItem * f / 256;  // their scales
-        const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(dd) + row0 * (f / 16);
-        if (lane < spieces) cp_async16(b + kDnRowsPerItem * f + lane * 16, ssrc + lane * 16);
-        cp_async_commit();
+        dn_issue_item(ring + (size_t)st * item_bytes, dqs, dd,
+                      (size_t)s_act[locate(g, s_cb, s_n)] * dm + (size_t)qd * kDnRowsPerItem, f, lane);
     };
     auto compute = [&](int i, int st) {
         const int g = i / nq, qd = i - g * nq;
@@ -378,63 +175,13 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
         const int c0 = g - s_cb[a];
         const int pb = ALLP ? s_beg[a] : s_beg[a] + c0 * tcp;
         const int pe = ALLP ? s_end[a] : min(s_end[a], pb + tcp);
-        const unsigned char* b = ring + (size_t)st * item_bytes;
-        const __half* sc = reinterpret_cast<const __half*>(b + kDnRowsPerItem * f);
-        for (int pp = pb; pp < pe; pp += G) {
-            const int ng = min(G, pe - pp);
-            int hoff[G];
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2) hoff[g2] = (g2 < ng ? (ALLP ? (pp + g2) : (pp + g2 - pb)) : 0) * kTok4;
-            float acc[2][G];
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                for (int g2 = 0; g2 < G; ++g2) acc[rr][g2] = 0.f;
-#pragma unroll
-            for (int m = 0; m < KCH; ++m) {
-                const int c = hl + LPR * m;
-                if (c < nch) {
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int rl = sub * 2 + rr;
-                        const uint4 q = *reinterpret_cast<const uint4*>(b + (size_t)rl * f + c * 16);
-                        const float s = __half2float(sc[rl * (f / 32) + (c >> 1)]);
-#pragma unroll
-                        for (int g2 = 0; g2 < G; ++g2)
-                            if (g2 < ng)
-                                acc[rr][g2] = fmaf(s, chunk_dot(q, hs + hoff[g2] + m * 4 * LPR + hl, LPR), acc[rr][g2]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                for (int g2 = 0; g2 < G; ++g2) acc[rr][g2] = group_sum<LPR>(acc[rr][g2]);
-#pragma unroll
-            for (int g2 = 0; g2 < G; ++g2) {
-                if (g2 < ng && hl < 2) {
-                    const int o = qd * kDnRowsPerItem + sub * 2 + hl;  // lane 0 / 1 of the half: row 0 / 1
-                    const float y = hl == 0 ? acc[0][g2] : acc[1][g2];
-                    const int p = pp + g2;
-                    if (fuse) {
-                        int tok;
-                        float wgt;
-                        if (ALLP) {
-                            tok = s_ptok[p];
-                            wgt = s_pw[p];
-                        } else {
-                            tok = __ldcg(pair_tok + p);
-                            const int sl = __ldcg(pair_slot + p);
-                            const bool ok = tok >= 0 && tok < T && sl >= 0 && sl < k;
-                            wgt = ok ? __ldcg(wts + (size_t)tok * k + sl) : 0.f;
-                            tok = ok ? tok : -1;
-                        }
-                        if (tok >= 0) atomicAdd(out + (size_t)tok * dm + o, wgt * y);
-                    } else {
-                        out[(size_t)p * dm + o] = y;
-                    }
-                }
-            }
+        if constexpr (G == kMultiG) {
+            const unsigned char* b = ring + (size_t)st * item_bytes;
+            if (ALLP) dn_compute_multi<KCH>(b, qd, pb, pe, f, dm, hl, sub, hs, pb, s_ptok + pb, s_pw + pb, fuse, out);
+            else dn_compute_multi<KCH>(b, qd, pb, pe, f, dm, hl, sub, hs, 0, s_segtok, s_segw, fuse, out);
+        } else {
+            dn_compute_item<KCH, G, ALLP>(ring + (size_t)st * item_bytes, qd, pb, pe, f, dm, k, T, hl, sub, hs,
+                                          s_ptok, s_pw, pair_tok, pair_slot, wts, fuse, out);
         }
     };
 
@@ -479,10 +226,17 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
             const int pb = s_beg[a] + (g - s_cb[a]) * tcp;
             const int pe = min(s_end[a], pb + tcp);
             __syncthreads();
+#pragma unroll 4
             for (int q = threadIdx.x; q < (pe - pb) * f4; q += kThreads) {
                 const int jj = q / f4, qq = q - jj * f4;
                 hs[jj * kTok4 + stage_idx<LPR>(qq)] =
                     __ldcg(reinterpret_cast<const float4*>(h) + (size_t)(pb + jj) * f4 + qq);
+            }
+            for (int j = threadIdx.x; j < pe - pb; j += kThreads) {
+                const int tok = __ldcg(pair_tok + pb + j), sl = __ldcg(pair_slot + pb + j);
+                const bool ok = tok >= 0 && tok < T && sl >= 0 && sl < k;
+                s_segtok[j] = ok ? tok : -1;
+                s_segw[j] = ok ? __ldcg(wts + (size_t)tok * k + sl) : 0.f;
             }
             __syncthreads();
             warp_stream<NSTG>(seg + warp, seg_end, NW, issue, compute);
@@ -541,14 +295,17 @@ template <int KCH>
 cudaError_t gateup_dispatch(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                             const int32_t* pair_tok, float* h, float* out_init, int residual, cudaStream_t s) {
     const int P = T * w.k;
-    const int tca = T <= 8 ? T : 8;
-    const bool alltok = T <= 8 && P <= kMaxStagedPairs;
+    const int tca = T <= kMultiG ? T : kMultiG;
+    const bool alltok = T <= kMultiG && P <= kMaxStagedPairs;
     // ring: 16 warps x 3 stages of one feature (gate + up rows) when the
     // activations are small, 12 warps otherwise
     if (T == 1 && alltok) return gateup_go<KCH, 1, true, 16, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
     if (T <= 2 && alltok) return gateup_go<KCH, 2, true, 16, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
-    if (alltok) return gateup_go<KCH, 4, true, 12, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
-    return gateup_go<KCH, 4, false, 12, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
+    // 3+ tokens: items of up to kMultiG pairs (a bucket holds at most T <= 8
+    // pairs when every token is staged, else chunks of tca = 8)
+    if (alltok)
+        return gateup_go<KCH, kMultiG, true, 12, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
+    return gateup_go<KCH, kMultiG, false, 12, 3>(x, T, w, offsets, pair_tok, h, out_init, residual, tca, s);
 }
 
 template <int KCH, int G, bool ALLP, int NW, int NSTG>
@@ -571,8 +328,12 @@ cudaError_t down_dispatch(const float* h, int T, const moe_layer_w& w, const int
     const bool allp = (size_t)P * tok_bytes <= 48 * 1024 && P <= kMaxStagedPairs;
     if (T == 1 && allp)
         return down_go<KCH, 1, true, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, P, s);
-    if (allp) return down_go<KCH, 4, true, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, P, s);
-    return down_go<KCH, 4, false, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, 8, s);
+    if (T <= 2 && allp) return down_go<KCH, 4, true, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, P, s);
+    // 3+ tokens: items of up to kMultiG pairs (whole buckets of <= T <= 8
+    // pairs when every pair's h is staged, else chunks of tcp = kMultiG)
+    if (allp && T <= kMultiG)
+        return down_go<KCH, kMultiG, true, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, P, s);
+    return down_go<KCH, kMultiG, false, 16, 3>(h, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, kMultiG, s);
 }
 
 }  // namespace

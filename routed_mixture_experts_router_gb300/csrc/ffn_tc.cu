@@ -75,16 +75,6 @@ __device__ __forceinline__ f32x2 f2_pack(float a, float b) {
 __device__ __forceinline__ void f2_unpack(f32x2 v, float& a, float& b) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
 }
-__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
-    f32x2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
-    f32x2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 // two fp32 -> bf16x2 (round to nearest even); `lo` lands in the low half
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     uint32_t r;
@@ -92,21 +82,30 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return r;
 }
 
-// 16 int8 (one 16-byte word) times scale d -> 16 bf16 (two 16-byte words).
-__device__ __forceinline__ void dequant16(uint4 q, float d, uint4& o0, uint4& o1) {
-    const f32x2 bias = 0xCB000080CB000080ull;  // (-(2^23 + 128), -(2^23 + 128))
-    const f32x2 dd = f2_pack(d, d);
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// 16 int8 (one 16-byte word) times scale d -> 16 bf16 (two 16-byte words),
+// each w = q * d computed exactly in fp32 and then rounded to bf16 (RNE).
+// The byte u = q + 128 is placed in bits 8..15 of the float 2^15, giving
+// v = 32768 + u exactly; one FMA v * d + c with c = -(32768 + 128) * d (exact:
+// a 9-bit integer times an 11-bit fp16 value) yields (u - 128) * d = q * d,
+// whose 19 significant bits are exact, so the FMA's single rounding is exact.
+__device__ __forceinline__ void dequant16(uint4 q, f32x2 dd, f32x2 cc, uint4& o0, uint4& o1) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint32_t r[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const uint32_t u = w[m] ^ 0x80808080u;
-        f32x2 lo = f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
-        f32x2 hi = f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
-        lo = f2_mul(f2_add(lo, bias), dd);  // q exact, q*d exact in fp32
-        hi = f2_mul(f2_add(hi, bias), dd);
+        const f32x2 lo = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
+                                        __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
+                                dd, cc);
+        const f32x2 hi = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7524)),
+                                        __uint_as_float(__byte_perm(u, 0x47000000u, 0x7534))),
+                                dd, cc);
         float a, b, c, e;
         f2_unpack(lo, a, b);
         f2_unpack(hi, c, e);
@@ -324,13 +323,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
             const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
             const size_t srow = (size_t)(U.e * p.rows + U.m0 + r) * nbk;
-            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1
-            float dc[NMAT][2], dn[NMAT][2];
+            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1;
+            // fetched two raw stages ahead (d0: stage kr, d1: kr + 1, d2: kr + 2)
+            float s0[NMAT][2], s1[NMAT][2], s2[NMAT][2];
 #pragma unroll
             for (int mat = 0; mat < NMAT; ++mat) {
                 const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) dc[mat][j] = ldg_half(dp + srow + 2 * j + hf);
+                for (int j = 0; j < 2; ++j) {
+                    s0[mat][j] = ldg_half(dp + srow + 2 * j + hf);
+                    s1[mat][j] = kr_n > 1 ? ldg_half(dp + srow + 4 + 2 * j + hf) : 0.f;
+                }
             }
             for (int kr = 0; kr < kr_n; ++kr) {
 #pragma unroll
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
-                        dn[mat][j] = (kr + 1 < kr_n) ? ldg_half(dp + srow + 4 * (kr + 1) + 2 * j + hf) : 0.f;
+                        s2[mat][j] = (kr + 2 < kr_n) ? ldg_half(dp + srow + 4 * (kr + 2) + 2 * j + hf) : 0.f;
                 }
                 const int rs = rc % kRS;
                 if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) break;
@@ -349,11 +352,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int mat = 0; mat < NMAT; ++mat) {
                         const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
                         unsigned char* at = As + (s * NMAT + mat) * kTile;
+                        const float d = j == 0 ? s0[mat][0] : s0[mat][1];
+                        const f32x2 dd = f2_pack(d, d);
+                        const f32x2 cc = f2_pack(-32896.0f * d, -32896.0f * d);
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + 2 * hf + i));
                             uint4 o0, o1;
-                            dequant16(q, dc[mat][j], o0, o1);
+                            dequant16(q, dd, cc, o0, o1);
                             *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i)) = o0;
                             *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i + 1)) = o1;
                         }
@@ -368,8 +374,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++rc;
 #pragma unroll
                 for (int mat = 0; mat < NMAT; ++mat) {
-                    dc[mat][0] = dn[mat][0];
-                    dc[mat][1] = dn[mat][1];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        s0[mat][j] = s1[mat][j];
+                        s1[mat][j] = s2[mat][j];
+                    }
                 }
                 if (s_abort) break;
             }

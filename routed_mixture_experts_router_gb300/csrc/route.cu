@@ -9,13 +9,15 @@
 // its lanes split K with coalesced 16-byte loads, so the 1 MiB router matrix
 // streams through 16 SMs in parallel even at T = 1.  Logits land in the
 // leader CTA's shared memory (distributed shared memory), and after one
-// cluster barrier the leader's warps run a warp-shuffle top-k, one warp per
-// token.  No global scratch, no atomics, no inter-CTA spin: deterministic.
+// cluster barrier the leader's threads rank the logits (top-k by rank, one
+// thread per (token, expert) candidate).  No global scratch, no atomics, no
+// inter-CTA spin: deterministic.
 #include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
 #include "pipeline.cuh"
+#include "route_warp.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -27,122 +29,6 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / kWarp;
 constexpr int kRouteUnroll = 8;  // float4 loads in flight per lane per step
 
-// Top-k over E (<= 256) logits of one token by one warp.  Lane l holds the
-// logits of experts l, l+32, ...  Each round takes the warp-wide maximum,
-// ties to the lower expert id; the winner is marked taken.  Round s's winner
-// goes to slot s.  Weights: exp(l_s - l_0) / sum over the selection.
-__device__ void topk_warp(const float* lg, const float* bias, int E, int k, int32_t* idx_out, float* w_out,
-                          int32_t* s_idx) {
-    const int lane = threadIdx.x & 31;
-    float v[MOE_MAX_EXPERTS / 32];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E) {
-            v[j] = lg[e] + (bias ? __ldg(bias + e) : 0.0f);
-        } else {
-            v[j] = -INFINITY;
-            taken |= 1u << j;
-        }
-    }
-    float my_v = 0.0f, vmax = 0.0f;
-    int my_e = 0;
-    for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
-            // experts grow with j inside a lane, so strict > keeps the lower id
-            if (!((taken >> j) & 1u) && (be == 0x7fffffff || v[j] > bv)) {
-                bv = v[j];
-                be = lane + 32 * j;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (lane == (be & 31)) taken |= 1u << (be >> 5);
-        if (lane == s) {
-            my_v = bv;
-            my_e = be;
-        }
-        if (s == 0) vmax = bv;
-    }
-    const float num = (lane < k) ? expf(my_v - vmax) : 0.0f;
-    const float den = warp_sum(num);
-    if (lane < k) {
-        idx_out[lane] = my_e;
-        w_out[lane] = num / den;
-        if (s_idx) s_idx[lane] = my_e;
-    }
-}
-
-// Compact expert grouping of T <= 32 tokens by one warp (fused into the
-// router when one cluster holds every token).  Lane t owns token t; ballots
-// over the tokens' expert bitmaps give, for each expert e, the set M[e] of
-// tokens that picked it; offsets are the exclusive scan of |M[e]| and pair
-// (t, s) lands at offsets[e] + |M[e] & tokens below t|: stable in
-// (token, slot) order, no atomics.
-__device__ void bucket_warp(const int32_t* s_idx, int T, int k, int E, int* s_off, uint32_t* s_m,
-                            int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot, int32_t* pos) {
-    const int lane = threadIdx.x & 31;
-    uint32_t bm[MOE_MAX_EXPERTS / 32];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
-    if (lane < T) {
-        for (int s = 0; s < k; ++s) {
-            const int e = s_idx[lane * k + s];
-#pragma unroll
-            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                if (j == (e >> 5)) bm[j] |= 1u << (e & 31);
-        }
-    }
-    const int words = (E + 31) >> 5;
-    int run = 0;
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
-        if (j < words) {
-            uint32_t mine = 0;
-#pragma unroll 8
-            for (int b = 0; b < 32; ++b) {
-                const uint32_t m = __ballot_sync(0xffffffffu, (bm[j] >> b) & 1u);
-                if (lane == b) mine = m;
-            }
-            const int e = 32 * j + lane;
-            const int cnt = (e < E) ? __popc(mine) : 0;
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            s_off[e] = run + incl - cnt;
-            s_m[e] = mine;
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-    }
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) offsets[e] = s_off[e];
-    if (lane == 0) offsets[E] = run;
-    if (lane < T) {
-        const uint32_t below = (1u << lane) - 1u;
-        for (int s = 0; s < k; ++s) {
-            const int e = s_idx[lane * k + s];
-            const int p = s_off[e] + __popc(s_m[e] & below);
-            pair_tok[p] = lane;
-            pair_slot[p] = s;
-            pos[lane * k + s] = p;
-        }
-    }
-}
-
 template <int TT>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ x,
                                                               const float* __restrict__ Wr,
@@ -152,8 +38,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
                                                               int32_t* offsets, int32_t* pair_tok,
                                                               int32_t* pair_slot, int32_t* pos) {
     __shared__ int32_t s_idx[TT * MOE_MAX_TOPK];
-    __shared__ int s_off[MOE_MAX_EXPERTS];
-    __shared__ uint32_t s_m[MOE_MAX_EXPERTS];
+    __shared__ float s_val[TT * MOE_MAX_TOPK];
     extern __shared__ float4 route_smem[];
     float4* xs = route_smem;                                   // [TT][dm/4]
     float* lg = reinterpret_cast<float*>(route_smem + TT * (dm / 4));  // [TT][e_stride]
@@ -218,14 +103,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     }
     cluster.sync();  // all logits of the tile are in the leader's shared memory
     if (c == 0) {
+        // top-k by rank over the whole CTA; with one tile holding every token
+        // the bucketing is fused (pair positions and offsets, also by rank)
         const bool fuse_bucket = offsets != nullptr && gridDim.y == 1;
-        for (int t = warp; t < nt; t += kRouteWarps)
-            topk_warp(lg + t * e_stride, bias, E, k, idx + (size_t)(t0 + t) * k, wts + (size_t)(t0 + t) * k,
-                      fuse_bucket ? s_idx + t * k : nullptr);
-        if (fuse_bucket) {
-            __syncthreads();
-            if (warp == 0) bucket_warp(s_idx, nt, k, E, s_off, s_m, offsets, pair_tok, pair_slot, pos);
+        prep_logits(lg, e_stride, nt, E, bias, kRouteThreads);
+        __syncthreads();
+        topk_rank_block(lg, e_stride, nt, E, k, kRouteThreads, s_idx, s_val);
+        __syncthreads();
+        const int P = nt * k;
+        for (int q = threadIdx.x; q < P; q += kRouteThreads) {
+            idx[(size_t)t0 * k + q] = s_idx[q];
+            wts[(size_t)t0 * k + q] = topk_weight(s_val, q, k);
+            if (fuse_bucket) {
+                const int r = pair_rank(s_idx, P, q);
+                pair_tok[r] = q / k;
+                pair_slot[r] = q - (q / k) * k;
+                pos[q] = r;
+            }
         }
+        if (fuse_bucket) bucket_offsets(s_idx, P, E, kRouteThreads, offsets);
     }
 }
 
@@ -297,10 +193,152 @@ int route_cluster_size(int E, size_t smem) {
 
 }  // namespace
 
+// ------------------------------------------------------------ large batches
+// Router logits as a split-K fp32 GEMM: one cluster of kGemmCl CTAs per tile
+// of kGemmTok tokens; CTA c accumulates K slice c for all experts with 4x EPT
+// register tiles over transposed shared-memory chunks of x and Wr, then the
+// cluster sums the slices through distributed shared memory in a fixed order
+// (deterministic) and each CTA runs the top-k of its share of the tokens.
+constexpr int kGemmTok = 32;
+constexpr int kGemmCl = 8;
+constexpr int kGemmKc = 32;
+constexpr int kGemmThreads = 256;
+
+template <int EPT>
+__global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* __restrict__ x,
+                                                                  const float* __restrict__ Wr,
+                                                                  const float* __restrict__ bias, int T, int dm,
+                                                                  int E, int k, int32_t* __restrict__ idx,
+                                                                  float* __restrict__ wts) {
+    constexpr int EP = 32 * EPT;  // padded expert count
+    __shared__ __align__(16) float xs[kGemmKc][kGemmTok];
+    __shared__ __align__(16) float ws[kGemmKc][EP];
+    __shared__ __align__(16) float part[kGemmTok][EP];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int c = static_cast<int>(cluster.block_rank());
+    const int t0 = blockIdx.y * kGemmTok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tg = tid & 7, eg = tid >> 3;  // tokens 4tg..4tg+3, experts EPT*eg..
+    const int kslice = dm / kGemmCl;
+    const int kbeg = c * kslice;
+    const int nch = kslice / kGemmKc;
+
+    // loaders: x chunk [32 tok][32 k] -> xs[k][tok]; Wr chunk [EP][32 k] -> ws[k][e]
+    const int lt = tid & 31, lk4 = tid >> 5;  // x: token lt, k quad lk4 (0..7)
+    float4 xr = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 wr[EPT];
+    auto load = [&](int ch) {
+        const int kk = kbeg + ch * kGemmKc;
+        const int t = t0 + lt;
+        xr = (t < T) ? __ldcg(reinterpret_cast<const float4*>(x + (size_t)t * dm + kk) + lk4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const int e = (tid & 31) + 32 * j;  // expert row, k quad = tid >> 5
+            const float4* src = reinterpret_cast<const float4*>(Wr + (size_t)e * dm + kk) + (tid >> 5);
+            wr[j] = (e < E) ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    pdl_wait();  // x is written by earlier kernels
+    load(0);
+    float acc[4][EPT];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+        __syncthreads();  // previous chunk consumed
+        xs[lk4 * 4 + 0][lt] = xr.x;
+        xs[lk4 * 4 + 1][lt] = xr.y;
+        xs[lk4 * 4 + 2][lt] = xr.z;
+        xs[lk4 * 4 + 3][lt] = xr.w;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const int e = (tid & 31) + 32 * j, kq = tid >> 5;
+            ws[kq * 4 + 0][e] = wr[j].x;
+            ws[kq * 4 + 1][e] = wr[j].y;
+            ws[kq * 4 + 2][e] = wr[j].z;
+            ws[kq * 4 + 3][e] = wr[j].w;
+        }
+        __syncthreads();
+        if (ch + 1 < nch) load(ch + 1);  // next chunk in flight during the FMAs
+#pragma unroll 8
+        for (int kk = 0; kk < kGemmKc; ++kk) {
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][tg * 4]);
+            float wv[EPT];
+#pragma unroll
+            for (int j = 0; j < EPT; j += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(&ws[kk][eg * EPT + j]);
+                wv[j] = q.x;
+                wv[j + 1] = q.y;
+                wv[j + 2] = q.z;
+                wv[j + 3] = q.w;
+            }
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xa[i], wv[j], acc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) part[tg * 4 + i][eg * EPT + j] = acc[i][j];
+    cluster.sync();  // every K slice is in its CTA's shared memory
+    // CTA c owns tokens c*4 .. c*4+3 of the tile: sum their logits over the
+    // K slices in a fixed order (deterministic), then rank them
+    constexpr int kOwn = kGemmTok / kGemmCl;
+    __shared__ int32_t s_sel[kOwn * MOE_MAX_TOPK];
+    __shared__ float s_val[kOwn * MOE_MAX_TOPK];
+    float* lg = &xs[0][0];  // reuse: [kOwn][EP] logits (kOwn * EP <= kGemmKc * kGemmTok)
+    const int tb = t0 + c * kOwn;
+    const int nt = min(kOwn, max(0, T - tb));
+    for (int i = tid; i < kOwn * EP; i += kGemmThreads) {
+        const int tl = c * kOwn + i / EP, e = i % EP;
+        float s = 0.f;
+        for (int r = 0; r < kGemmCl; ++r) s += cluster.map_shared_rank(&part[0][0], r)[tl * EP + e];
+        lg[i] = s;
+    }
+    __syncthreads();
+    prep_logits(lg, EP, nt, E, bias, kGemmThreads);
+    __syncthreads();
+    topk_rank_block(lg, EP, nt, E, k, kGemmThreads, s_sel, s_val);
+    __syncthreads();
+    for (int q = tid; q < nt * k; q += kGemmThreads) {
+        idx[(size_t)tb * k + q] = s_sel[q];
+        wts[(size_t)tb * k + q] = topk_weight(s_val, q, k);
+    }
+    cluster.sync();  // no CTA leaves while others still read its partial sums
+}
+
+template <int EPT>
+cudaError_t launch_route_gemm(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts,
+                              cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kGemmCl, (T + kGemmTok - 1) / kGemmTok, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kGemmCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, route_gemm_kernel<EPT>, x, w.router_w, w.router_bias, T, w.d_model, w.E, w.k,
+                              idx, wts);
+}
+
 cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts, int32_t* offsets,
                          int32_t* pair_tok, int32_t* pair_slot, int32_t* pos, bool* bucketed, cudaStream_t s) {
     if (bucketed) *bucketed = false;
     if (T == 0) return cudaSuccess;
+    if (T >= 128 && w.E <= 128 && w.d_model % (kGemmCl * kGemmKc) == 0)
+        return launch_route_gemm<4>(x, T, w, idx, wts, s);
     // tokens per tile: bounded so the x tile stays within 96 KB of shared memory
     int tt = T >= 8 ? 8 : (T >= 4 ? 4 : (T >= 2 ? 2 : 1));
     while (tt > 1 && (size_t)tt * w.d_model * sizeof(float) > 96 * 1024) tt >>= 1;
