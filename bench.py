@@ -454,6 +454,174 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def run_stack(args, ws, rank, local):
+    """The 48-layer stack: every layer resident, one CUDA graph per step running
+    x_{l+1} = x_l + MoE_l(x_l) through all layers (residual chaining through two
+    ping-pong buffers).  tokens/s = T / t_stack."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
+    tc_path = act == binding.MOE_ACT_BF16 and wl.T * wl.k >= 128
+    binding.load()
+    L = wl.layers
+    layers, host0 = [], None
+    for l in range(L):
+        w = synth.make_layer(wl, l, dev)
+        if l == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
+        layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
+                                                w["Wr"], w["bias"]))
+        del w
+    x0 = synth.make_x(wl, dev, step=0)
+    bufs = [torch.empty_like(x0), torch.empty_like(x0)]
+    wsb = binding.workspace(wl.T, layers[0], act, 0, dev)
+    offs = [torch.empty(wl.E + 1, dtype=torch.int32, device=dev) for _ in range(L)]
+    torch.cuda.synchronize()  # everything above was made on the default stream
+    stream = torch.cuda.Stream(device=dev)
+
+    def stack_call(record_offsets=False):
+        bufs[0].copy_(x0)  # this step's input
+        for l in range(L):
+            binding.layer_forward(bufs[l % 2], layers[l], act, 0, True, out=bufs[(l + 1) % 2], ws=wsb,
+                                  offsets_out=offs[l] if record_offsets else None)
+
+    with torch.cuda.stream(stream):
+        stack_call(record_offsets=True)
+        stack_call()
+    torch.cuda.synchronize()
+    g = new_graph()
+    with torch.cuda.graph(g, stream=stream):
+        stack_call()
+    torch.cuda.synchronize()
+    n_active = [int((np.diff(o.cpu().numpy()) > 0).sum()) for o in offs]
+    xbytes = wl.T * wl.d_model * 4
+    step_bytes = sum(n * expert_bytes(wl) + 2 * xbytes + wl.E * wl.d_model * 4 for n in n_active)
+    kn = graph_kernel_nodes(g)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        t_soak = time.time()
+        while time.time() - t_soak < args.soak:
+            g.replay()
+            torch.cuda.synchronize()
+        t_clk0 = time.time()
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        t_clk1 = time.time()
+    ms_local = e0.elapsed_time(e1)
+    sampler.stop()
+    clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
+    ms = max_over_ranks(ms_local, ws, dev)
+    tokens = args.steps * wl.T * ws
+    value = tokens / (ms / 1e3)
+
+    # dominant kernel: the expert FFN of each layer, timed alone (routing first, outside the events)
+    P = wl.T * wl.k
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
+    wts = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+    pt = torch.empty(P, dtype=torch.int32, device=dev)
+    ps = torch.empty(P, dtype=torch.int32, device=dev)
+    po = torch.empty(P, dtype=torch.int32, device=dev)
+    off = torch.empty(wl.E + 1, dtype=torch.int32, device=dev)
+    out2 = torch.empty_like(x0)
+    Lb = binding.load()
+    st = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
+    ffn_ms, ffn_alg = [], []
+    with torch.cuda.stream(stream):
+        for rep in range(3):
+            for l in range(L):
+                binding._check("moe_route", Lb.moe_route(binding._ptr(x0), wl.T, layers[l].ref(), binding._ptr(idx),
+                                                         binding._ptr(wts), binding.ctypes.c_void_p(st())))
+                binding._check("moe_bucket", Lb.moe_bucket(binding._ptr(idx), wl.T, wl.k, wl.E, binding._ptr(off),
+                                                           binding._ptr(pt), binding._ptr(ps), binding._ptr(po), None,
+                                                           binding.ctypes.c_void_p(st())))
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                binding.expert_ffn_q8(x0, layers[l], off, pt, ps, wts, act, True, True, ws=wsb, out=out2)
+                b.record(stream)
+                torch.cuda.synchronize()
+                if rep > 0:
+                    ffn_ms.append(a.elapsed_time(b))
+                    na = int((np.diff(off.cpu().numpy()) > 0).sum())
+                    ffn_alg.append(na * expert_bytes(wl) + 2 * xbytes)
+    peaks = load_peaks()
+    ffn_ms_mean = float(np.mean(ffn_ms))
+    alg = float(np.mean(ffn_alg))
+    achieved = alg / (ffn_ms_mean / 1e3) / 1e9
+    roofline = {"kernel": ("moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)" if tc_path
+                           else "moe_expert_ffn_q8 (gate/up + down, Q8_0 fused, combine fused)"),
+                "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": alg, "launch_ms": ffn_ms_mean, "traffic": None,
+                "timed_over": f"{len(ffn_ms)} launches, every layer of the stack"}
+    if tc_path:
+        flops = 2.0 * wl.T * wl.k * 3 * wl.d_model * wl.d_ff
+        tf = flops / (ffn_ms_mean / 1e3) / 1e12
+        roofline["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                              "frac": tf / peaks["bf16_tflops"], "flops_per_launch": flops}
+
+    # end to end: pinned x in, the stack, the final hidden state out
+    xh = x0.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            x0.copy_(xh, non_blocking=True)
+            g.replay()
+            oh.copy_(bufs[L % 2], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+
+    cpu_base = None
+    if host0 is not None:
+        xa = synth.make_x(wl, "cpu", step=1000, T=256).double().numpy()
+        tps, done, threads, secs = oracle_tokens_per_s(wl, host0, xa, budget_s=args.cpu_budget)
+        model, ncpu = cpu_info()
+        cpu_base = {"value": tps / L, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                    "sample": f"layer 0 of the stack timed on {done} independent tokens in {secs:.1f} s; "
+                              f"stack rate = layer rate / {L} (extrapolated), {model}, {ncpu} host cores"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
+            "data": "synthetic (seeded, qwen3_moe geometry, random-init Q8_0)",
+            "config": {"workload": f"{wl.name}: {L}-layer MoE stack with residual, T={wl.T}, d_model={wl.d_model}, "
+                                   f"d_ff={wl.d_ff}, E={wl.E}, top-{wl.k}, Zipf router bias, "
+                                   f"{'bf16' if tc_path else 'f32'} expert inputs",
+                       "tokens_per_step": wl.T, "layers": L,
+                       "l2": f"inputs larger than L2: {L} resident layers x 128 experts x 5013504 B",
+                       "parallelism": f"replicas x{ws}", "graph": f"one CUDA graph per step ({L} layers)"},
+            "stack_hbm_gbs": step_bytes / (ms_local / args.steps / 1e3) / 1e9,
+            "roofline": roofline, "cpu_baseline": cpu_base,
+            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
+                    "d2h_bytes_per_step": xbytes},
+            "gpu_launches": None if kn is None else kn * args.steps,
+            "gpu_launches_source": "kernel nodes of the captured step graph" if kn is not None
+            else "graph introspection unavailable",
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def load_traffic(key: str):
     """DRAM bytes per launch from a committed ncu capture, or None when the
     kernel source changed since the counters were taken."""
@@ -497,6 +665,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, ws, rank)
+        if synth.WORKLOADS[args.workload].layers > 1:
+            return run_stack(args, ws, rank, local)
         return run_ours(args, ws, rank, local)
     finally:
         if ws > 1:

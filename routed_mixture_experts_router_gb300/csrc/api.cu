@@ -88,8 +88,9 @@ int check_device() {
 
 // Expert path: bf16 activations -> tcgen05 kernels when the batch fills at
 // least one 128-pair MMA tile (smaller batches run the fp32 path, which is
-// more accurate and memory-bound anyway); fp32 -> the streaming kernels where
-// the geometry allows, the per-expert-CTA kernels otherwise.
+// more accurate and memory-bound anyway); fp32 -> for 3+ tokens the
+// lane-per-row kernels, for 1-2 tokens the streaming kernels, where the
+// geometry allows; the per-expert-CTA kernels otherwise.
 cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, const int32_t* offsets,
                        const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse, float* out,
                        int residual, char* ws, const WsLayout& L, int32_t* status, cudaStream_t s) {
@@ -98,6 +99,8 @@ cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, con
         return launch_ffn_tc(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual,
                              reinterpret_cast<__nv_bfloat16*>(ws + L.xb), reinterpret_cast<__nv_bfloat16*>(h),
                              status, s);
+    if (ffn_rows_supported(w, T))
+        return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
     if (ffn_stream_supported(w))
         return launch_ffn_stream(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, status, s);
     return launch_ffn_f32(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);

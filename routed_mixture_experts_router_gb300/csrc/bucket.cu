@@ -183,12 +183,140 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
     if (tid == 0 && s_bad) flag_status(status, MOE_STATUS_BAD_INDEX);
 }
 
+// Same result, for batches whose per-expert pair bitmaps fit in shared
+// memory: pair p = t*k + s sets bit p of its expert's bitmap M[e]; one warp
+// per expert turns the bitmap into word prefix counts (popcount + warp scan)
+// and the bucket size; pair p then lands at
+//   offsets[e] + (pairs of e in words below p/32) + popc(M[e][p/32] & bits below p).
+// Every phase is parallel over pairs, words or experts (no serial ballot
+// transposes), and the order is the same stable (token, slot) order.
+__global__ void __launch_bounds__(kBucketThreads) bucket_mask_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                                     int E, int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ pair_tok,
+                                                                     int32_t* __restrict__ pair_slot,
+                                                                     int32_t* __restrict__ pos, int32_t* status) {
+    __shared__ int s_cnt[MOE_MAX_EXPERTS];
+    __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+    __shared__ int s_wsum[kBucketWarps];
+    __shared__ int s_bad;
+    extern __shared__ uint32_t bucket_dyn[];
+    const int P = T * k;
+    const int W = (P + 31) >> 5;
+    uint32_t* s_mask = bucket_dyn;                                          // [E][W]
+    uint16_t* s_pre = reinterpret_cast<uint16_t*>(bucket_dyn + (size_t)E * W);  // [E][W] pairs in earlier words
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();  // idx written by the router
+    pdl_launch_dependents();
+    for (int i = tid; i < E * W; i += kBucketThreads) s_mask[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // 1. one token per thread: validate its ids, drop repeats, set the bits
+    for (int t = tid; t < T; t += kBucketThreads) {
+        uint32_t seen[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) seen[j] = 0;
+        int ids[MOE_MAX_TOPK];
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) ids[s] = s < k ? __ldcg(idx + (size_t)t * k + s) : -1;
+#pragma unroll
+        for (int s = 0; s < MOE_MAX_TOPK; ++s) {
+            if (s >= k) break;
+            const int e = ids[s];
+            bool ok = e >= 0 && e < E;
+            if (ok) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                    if (j == (e >> 5)) word = seen[j];
+                ok = !(word & (1u << (e & 31)));
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                    if (j == (e >> 5)) seen[j] |= 1u << (e & 31);
+            }
+            if (!ok) {
+                s_bad = 1;
+                continue;
+            }
+            const int p = t * k + s;
+            atomicOr(&s_mask[(size_t)e * W + (p >> 5)], 1u << (p & 31));
+        }
+    }
+    __syncthreads();
+    // 2. per expert (one warp each): word prefix counts and the bucket size
+    for (int e = warp; e < E; e += kBucketWarps) {
+        int carry = 0;
+        for (int w0 = 0; w0 < W; w0 += 32) {
+            const int w = w0 + lane;
+            const int c = w < W ? __popc(s_mask[(size_t)e * W + w]) : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (w < W) s_pre[(size_t)e * W + w] = static_cast<uint16_t>(carry + incl - c);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_cnt[e] = carry;
+    }
+    __syncthreads();
+    // 3. offsets: exclusive scan of the bucket sizes (E <= 256: 8 warps + fix-up)
+    if (tid < MOE_MAX_EXPERTS) {
+        const int v = tid < E ? s_cnt[tid] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        s_off[tid] = incl - v;  // exclusive within the warp for now
+    }
+    __syncthreads();
+    if (tid < MOE_MAX_EXPERTS) {
+        int add = 0;
+        for (int w = 0; w < (tid >> 5); ++w) add += s_wsum[w];
+        if (tid < E) s_off[tid] += add;
+        if (tid == E - 1) s_off[E] = s_off[tid] + s_cnt[tid];
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += kBucketThreads) offsets[e] = s_off[e];
+    // 4. positions: one pair per thread (unrolled: the id loads overlap)
+#pragma unroll 8
+    for (int p = tid; p < P; p += kBucketThreads) {
+        const int e = __ldcg(idx + p);
+        int ps = -1;
+        if (e >= 0 && e < E) {
+            const uint32_t m = s_mask[(size_t)e * W + (p >> 5)];
+            if (m & (1u << (p & 31)))  // kept (not an invalid or repeated id)
+                ps = s_off[e] + s_pre[(size_t)e * W + (p >> 5)] + __popc(m & ((1u << (p & 31)) - 1u));
+        }
+        pos[p] = ps;
+        if (ps >= 0) {
+            pair_tok[ps] = p / k;
+            pair_slot[ps] = p - (p / k) * k;
+        }
+    }
+    if (tid == 0 && s_bad) flag_status(status, MOE_STATUS_BAD_INDEX);
+}
+
+size_t bucket_mask_smem(int T, int k, int E) {
+    const size_t W = ((size_t)T * k + 31) / 32;
+    return (size_t)E * W * (sizeof(uint32_t) + sizeof(uint16_t));
+}
+
+constexpr size_t kBucketMaskCap = 200 * 1024;
+
 }  // namespace
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok,
                           int32_t* pair_slot, int32_t* pos, int32_t* status, cudaStream_t s) {
-    const size_t smem = (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t);
-    cudaError_t err = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t msmem = bucket_mask_smem(T, k, E);
+    const bool use_mask = (size_t)T * k <= 65535 && msmem <= kBucketMaskCap;  // word prefixes fit 16 bits
+    const size_t smem = use_mask ? msmem : (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t);
+    auto kern = use_mask ? bucket_mask_kernel : bucket_kernel;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
@@ -200,7 +328,7 @@ cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offs
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bucket_kernel, idx, T, k, E, offsets, pair_tok, pair_slot, pos, status);
+    return cudaLaunchKernelEx(&cfg, kern, idx, T, k, E, offsets, pair_tok, pair_slot, pos, status);
 }
 
 }  // namespace moe

@@ -86,6 +86,10 @@ cudaError_t launch_ffn_f32(const float* x, int T, const moe_layer_w& w, const in
 
 // Streaming (persistent, bulk-copy pipelined) fp32 expert path for shapes
 // with d_model, d_ff multiples of 64.
+bool ffn_rows_supported(const moe_layer_w& w, int T);
+cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
+                            const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
+                            float* out_or_ypairs, int residual, float* h, cudaStream_t s);
 bool ffn_stream_supported(const moe_layer_w& w);
 cudaError_t launch_ffn_stream(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                               const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,

@@ -41,13 +41,15 @@ __device__ __forceinline__ int stage_index(int q /* float4 index in the row */) 
 }
 
 // Index of the a-th expert with a non-empty bucket (-1 if none); one warp.
-__device__ __forceinline__ int find_active_expert(const int32_t* offsets, int E, int a, int* beg, int* end) {
+// Buckets are clamped into [0, P]: offsets that are not a valid bucketing
+// give wrong sums, never an out-of-range pair.
+__device__ __forceinline__ int find_active_expert(const int32_t* offsets, int E, int P, int a, int* beg, int* end) {
     const int lane = threadIdx.x & 31;
     int seen = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const int lo = e < E ? __ldg(offsets + e) : 0;
-        const int hi = e < E ? __ldg(offsets + e + 1) : 0;
+        const int lo = min(max(e < E ? __ldg(offsets + e) : 0, 0), P);
+        const int hi = min(max(e < E ? __ldg(offsets + e + 1) : 0, lo), P);
         const uint32_t act = __ballot_sync(0xffffffffu, hi > lo);
         const int n = __popc(act);
         if (a < seen + n) {
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2) gateup_f32_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
     const uint16_t* __restrict__ gd, const int8_t* __restrict__ uqs, const uint16_t* __restrict__ ud,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok, float* __restrict__ h,
-    float* __restrict__ out_init, int init_residual) {
+    float* __restrict__ out_init, int init_residual, int P) {
     extern __shared__ float4 gu_smem[];  // [TC][KCH*4*32] float4
     __shared__ int s_e, s_beg, s_end;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2) gateup_f32_kernel(
     }
     if (warp == 0) {
         int beg = 0, end = 0;
-        const int e = find_active_expert(offsets, E, blockIdx.y, &beg, &end);
+        const int e = find_active_expert(offsets, E, P, blockIdx.y, &beg, &end);
         if (lane == 0) {
             s_e = e;
             s_beg = beg;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2) down_f32_kernel(
     const int nch = f / 16;
     if (warp == 0) {
         int beg = 0, end = 0;
-        const int e = find_active_expert(offsets, E, blockIdx.y, &beg, &end);
+        const int e = find_active_expert(offsets, E, T * k, blockIdx.y, &beg, &end);
         if (lane == 0) {
             s_e = e;
             s_beg = beg;
@@ -296,7 +298,7 @@ cudaError_t launch_gateup(const float* x, int T, const moe_layer_w& w, const int
     if (err != cudaSuccess) return err;
     dim3 grid((w.d_ff + kFfnWarps - 1) / kFfnWarps, P < w.E ? P : w.E);
     kern<<<grid, kFfnThreads, smem, s>>>(x, T, w.d_model, w.d_ff, w.E, w.gate.qs, w.gate.d, w.up.qs, w.up.d, offsets,
-                                         pair_tok, h, out_init, residual);
+                                         pair_tok, h, out_init, residual, P);
     return cudaGetLastError();
 }
 

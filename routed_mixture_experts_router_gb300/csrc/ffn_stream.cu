@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
     float4* xs = reinterpret_cast<float4*>(gu_smem + (size_t)NW * NSTG * item_bytes);
 
     pdl_wait();  // routing / bucketing of this layer complete and visible
-    if (warp == 0) build_active(offsets, E, ALLTOK ? (1 << 30) : tca, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0) build_active(offsets, E, ALLTOK ? (1 << 30) : tca, P, s_act, s_beg, s_end, s_cb, &s_n);
     if (ALLTOK) {
         for (int p = threadIdx.x; p < P; p += kThreads) {
             const int t = __ldcg(pair_tok + p);
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
 
     // Offsets were written two kernels back (routing/bucketing) and were
     // complete before gate/up released this grid: Wd can stream at once.
-    if (warp == 0) build_active(offsets, E, ALLP ? (1 << 30) : tcp, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0) build_active(offsets, E, ALLP ? (1 << 30) : tcp, P, s_act, s_beg, s_end, s_cb, &s_n);
     __syncthreads();
     int lo, hi;
     item_range(s_cb[s_n] * nq, &lo, &hi);

@@ -17,13 +17,15 @@
 // the small, ragged token count is N) and up to 128 of its tokens (N, padded
 // to a multiple of 16).  Warp roles:
 //   warp 0       TMA producer: int8 weight tiles (128 rows x 128 K, 128-byte
-//                swizzle) into a raw ring; bf16 token tiles (N x 64 K) into
-//                the operand ring
+//                swizzle) into a raw ring
+//   warp 2       TMA producer: bf16 token tiles (N x 64 K) into the operand
+//                ring (separate, so the weight stream never waits on it)
 //   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, M=128,
 //                K=16 per instruction, into a double-buffered TMEM accumulator
-//   warps 4-11   dequantisation: thread = (row, half of K); int8 -> fp32
-//                exactly, times the block's fp16 scale, -> bf16 (RNE), written
-//                in the 128-byte-swizzled K-major layout the MMA reads
+//   warps 4-11   dequantisation: thread = (row, half of each 64-K operand
+//                stage); int8 -> fp32 exactly, times the block's fp16 scale,
+//                -> bf16 (RNE), written in the 128-byte-swizzled K-major
+//                layout the MMA reads
 //   warps 12-15  epilogue: tcgen05.ld of the accumulator (TMEM lane = row),
 //                SwiGLU -> bf16 h, or the weighted combine into out
 // Every mbarrier wait is bounded: past the deadline the CTA flags
@@ -46,7 +48,15 @@ constexpr int kBKR = 128;     // int8 K per raw stage (one 128-byte row)
 constexpr int kBK = 64;       // bf16 K per operand stage (one 128-byte row)
 constexpr int kBN = 128;      // max tokens per unit (MMA N)
 constexpr int kBRows = 32;    // token rows per TMA box
-constexpr int kRS = 2;        // raw ring stages
+// Ring depths.  The raw (int8) ring is what keeps HBM busy: at a few
+// microseconds of loaded latency a sustained ~45 GB/s per SM needs ~100 KB of
+// weights in flight per SM, so shared memory goes to raw stages first and the
+// operand (bf16) ring keeps only the depth the dequant -> MMA hand-off needs.
+template <int NMAT>
+struct TcRing {
+    static constexpr int RS = NMAT == 2 ? 3 : 6;  // raw stages (NMAT x 16 KB each)
+    static constexpr int AS = NMAT == 2 ? 2 : 3;  // operand stages (NMAT A tiles + one B tile)
+};
 constexpr int kTile = 16384;  // one 128 x 128-byte tile
 constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12;
 
@@ -122,15 +132,19 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 }
 
 // Active experts in id order (warp-wide); buckets cut into chunks of kBN pairs.
-__device__ void tc_build_active(const int32_t* offsets, int E, int* s_act, int* s_beg, int* s_end, int* s_cb,
+// Buckets clamped into [0, P] (offsets that are not a valid bucketing give
+// wrong sums, never an out-of-range pair).
+__device__ void tc_build_active(const int32_t* offsets, int E, int P, int* s_act, int* s_beg, int* s_end, int* s_cb,
                                 int* s_n) {
     const int lane = threadIdx.x & 31;
     int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
         const int e = 32 * j + lane;
-        lo[j] = e < E ? __ldcg(offsets + e) : 0;
-        hi[j] = e < E ? __ldcg(offsets + e + 1) : 0;
+        const int a = e < E ? __ldcg(offsets + e) : 0;
+        const int b = e < E ? __ldcg(offsets + e + 1) : 0;
+        lo[j] = min(max(a, 0), P);
+        hi[j] = min(max(b, lo[j]), P);
     }
     int n = 0, nc = 0;
 #pragma unroll
@@ -193,7 +207,8 @@ template <int NMAT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                   const __grid_constant__ CUtensorMap tm_b, TcParams p) {
-    constexpr int AS = NMAT == 2 ? 3 : 4;  // operand ring stages
+    constexpr int kRS = TcRing<NMAT>::RS;
+    constexpr int AS = TcRing<NMAT>::AS;
     constexpr uint32_t kTmemCols = NMAT * kBN * 2;
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[kRS], raw_empty[kRS], b_full[AS], a_full[AS], ab_empty[AS];
@@ -237,7 +252,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tmap(&tm_b);
     }
     pdl_wait();  // bucketing and the previous stage's activations are complete
-    if (warp == 2) tc_build_active(p.offsets, p.E, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 2) tc_build_active(p.offsets, p.E, p.T * p.k, s_act, s_beg, s_end, s_cb, &s_n);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -248,14 +263,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kr_n = p.K / kBKR;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+        // ------------------------------------------------- TMA producer: weights
+        // runs ahead of the dequant warps by up to kRS raw stages, independent
+        // of the operand ring (token tiles have their own producer, warp 2)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            uint32_t rc = 0, ac = 0;
+            uint32_t rc = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
                 const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
                 const int wrow = U.e * p.rows + U.m0;
-                const int nb = (U.N + kBRows - 1) / kBRows;
                 for (int kr = 0; kr < kr_n; ++kr) {
                     const int rs = rc % kRS;
                     if (!tc_wait(raw_empty + rs, ((rc / kRS) & 1) ^ 1, p.status, &s_abort)) break;
@@ -264,6 +280,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (NMAT == 2)
                         tma_load_2d_hint(raw + (rs * NMAT + 1) * kTile, &tm_a1, kr * kBKR, wrow, raw_full + rs, pol);
                     ++rc;
+                }
+            }
+            // drain: every issued copy has landed before the CTA can exit
+            for (uint32_t c = (rc > kRS ? rc - kRS : 0); c < rc; ++c) mbar_wait(raw_full + c % kRS, (c / kRS) & 1);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------- TMA producer: tokens
+        if (lane == 0) {
+            uint32_t ac = 0;
+            for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const int nb = (U.N + kBRows - 1) / kBRows;
+                for (int kr = 0; kr < kr_n && !s_abort; ++kr) {
                     for (int j = 0; j < 2; ++j) {
                         const int s = ac % AS;
                         if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
@@ -273,11 +302,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         U.p0 + bb * kBRows, b_full + s);
                         ++ac;
                     }
-                    if (s_abort) break;
                 }
             }
-            // drain: every issued copy has landed before the CTA can exit
-            for (uint32_t c = (rc > kRS ? rc - kRS : 0); c < rc; ++c) mbar_wait(raw_full + c % kRS, (c / kRS) & 1);
             for (uint32_t c = (ac > AS ? ac - AS : 0); c < ac; ++c) mbar_wait(b_full + c % AS, (c / AS) & 1);
         }
     } else if (warp == 1) {
@@ -317,42 +343,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
         // ---------------------------------------------------------------- dequantisation
         const int tq = (warp - kDqWarp0) * 32 + lane;
-        const int r = tq & (kBM - 1), hf = tq >> 7;  // row, half of each 64-K operand stage
+        const int r = tq & (kBM - 1), hf = tq >> 7;  // row, half (one Q8_0 block) of each 64-K operand stage
         const int nbk = p.K / 32;                    // scale blocks per row
         uint32_t rc = 0, ac = 0;
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
             const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
             const size_t srow = (size_t)(U.e * p.rows + U.m0 + r) * nbk;
-            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1;
-            // fetched two raw stages ahead (d0: stage kr, d1: kr + 1, d2: kr + 2)
-            float s0[NMAT][2], s1[NMAT][2], s2[NMAT][2];
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat) {
-                const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    s0[mat][j] = ldg_half(dp + srow + 2 * j + hf);
-                    s1[mat][j] = kr_n > 1 ? ldg_half(dp + srow + 4 + 2 * j + hf) : 0.f;
-                }
-            }
-            for (int kr = 0; kr < kr_n; ++kr) {
+            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1.
+            // Four register sets on rotating stages, each refilled (for stage
+            // kr + 4) right after its use: no move ever waits on a load, and
+            // every scale load has three raw stages (several microseconds) to
+            // land.  Raw fp16 bits, converted at the use.
+            unsigned short sa[NMAT][2], sb[NMAT][2], sc2[NMAT][2], sd[NMAT][2];
+            auto fetch = [&](int kr, unsigned short (&sc)[NMAT][2]) {
 #pragma unroll
                 for (int mat = 0; mat < NMAT; ++mat) {
-                    const uint16_t* dp = mat == 0 ? p.d0 : p.d1;
+                    const unsigned short* dp = reinterpret_cast<const unsigned short*>(mat == 0 ? p.d0 : p.d1);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        s2[mat][j] = (kr + 2 < kr_n) ? ldg_half(dp + srow + 4 * (kr + 2) + 2 * j + hf) : 0.f;
+                    for (int j = 0; j < 2; ++j) sc[mat][j] = kr < kr_n ? __ldg(dp + srow + 4 * kr + 2 * j + hf) : 0;
                 }
+            };
+            auto stage = [&](int kr, unsigned short (&sc)[NMAT][2]) -> bool {
                 const int rs = rc % kRS;
-                if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) break;
+                if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) return false;
                 for (int j = 0; j < 2; ++j) {
                     const int s = ac % AS;
-                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
+                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) return false;
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
                         const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
                         unsigned char* at = As + (s * NMAT + mat) * kTile;
-                        const float d = j == 0 ? s0[mat][0] : s0[mat][1];
+                        const float d = __half2float(__ushort_as_half(j == 0 ? sc[mat][0] : sc[mat][1]));
                         const f32x2 dd = f2_pack(d, d);
                         const f32x2 cc = f2_pack(-32896.0f * d, -32896.0f * d);
 #pragma unroll
@@ -372,16 +393,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty + rs);
                 ++rc;
-#pragma unroll
-                for (int mat = 0; mat < NMAT; ++mat) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        s0[mat][j] = s1[mat][j];
-                        s1[mat][j] = s2[mat][j];
-                    }
-                }
-                if (s_abort) break;
+                fetch(kr + 4, sc);
+                return !s_abort;
+            };
+            fetch(0, sa);
+            fetch(1, sb);
+            fetch(2, sc2);
+            fetch(3, sd);
+            bool ok = true;
+            for (int kr = 0; kr < kr_n && ok; kr += 4) {
+                ok = stage(kr, sa);
+                if (ok && kr + 1 < kr_n) ok = stage(kr + 1, sb);
+                if (ok && kr + 2 < kr_n) ok = stage(kr + 2, sc2);
+                if (ok && kr + 3 < kr_n) ok = stage(kr + 3, sd);
             }
+            if (!ok) break;
         }
     } else if (warp >= kEpWarp0) {
         // ---------------------------------------------------------------- epilogue
@@ -515,7 +541,8 @@ int tc_num_sms() {
 template <int NMAT, int EPI>
 cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const TcParams& p,
                       cudaStream_t s) {
-    constexpr int AS = NMAT == 2 ? 3 : 4;
+    constexpr int kRS = TcRing<NMAT>::RS;
+    constexpr int AS = TcRing<NMAT>::AS;
     const size_t smem = (size_t)(kRS * NMAT + AS * NMAT + AS) * kTile + 1024;
     auto kern = tc_ffn_kernel<NMAT, EPI>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

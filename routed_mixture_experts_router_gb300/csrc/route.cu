@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     cg::cluster_group cluster = cg::this_cluster();
     const int c = static_cast<int>(cluster.block_rank());
     const int t0 = blockIdx.y * kGemmTok;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int tg = tid & 7, eg = tid >> 3;  // tokens 4tg..4tg+3, experts EPT*eg..
     const int kslice = dm / kGemmCl;
     const int kbeg = c * kslice;

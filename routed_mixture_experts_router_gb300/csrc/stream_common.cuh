@@ -85,17 +85,21 @@ __device__ __forceinline__ int stage_idx(int q) {
 // list they imply: expert a's bucket is cut into chunks of at most `chunk`
 // pairs (the activations one pass stages in shared memory); s_cb[a] is the
 // index of a's first chunk and s_cb[n] the total.  All offsets are fetched in
-// one round trip, through L2 (they were written by an earlier kernel).
+// one round trip, through L2 (they were written by an earlier kernel, or come
+// from the caller).  Every bucket is clamped into [0, P]: offsets that are
+// not a valid bucketing give wrong sums, never an out-of-range pair.
 template <bool FROM_SMEM = false>
-__device__ void build_active(const int32_t* offsets, int E, int chunk, int* s_act, int* s_beg, int* s_end,
+__device__ void build_active(const int32_t* offsets, int E, int chunk, int P, int* s_act, int* s_beg, int* s_end,
                              int* s_cb, int* s_n) {
     const int lane = threadIdx.x & 31;
     int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
         const int e = 32 * j + lane;
-        lo[j] = e < E ? (FROM_SMEM ? offsets[e] : __ldcg(offsets + e)) : 0;
-        hi[j] = e < E ? (FROM_SMEM ? offsets[e + 1] : __ldcg(offsets + e + 1)) : 0;
+        const int a = e < E ? (FROM_SMEM ? offsets[e] : __ldcg(offsets + e)) : 0;
+        const int b = e < E ? (FROM_SMEM ? offsets[e + 1] : __ldcg(offsets + e + 1)) : 0;
+        lo[j] = min(max(a, 0), P);
+        hi[j] = min(max(b, lo[j]), P);
     }
     int n = 0, nc = 0;
 #pragma unroll

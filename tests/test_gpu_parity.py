@@ -24,8 +24,10 @@ SHAPES = [
     ("t2_k1", 2, 1024, 384, 64, 1, True),
     ("d4096", 9, 4096, 64, 24, 3, False),
     ("s256_t7", 7, 256, 256, 16, 4, True),    # streaming path, all tokens staged at once
-    ("t12", 12, 1024, 512, 64, 6, True),      # streaming path, per-bucket activation chunks
+    ("t12", 12, 1024, 512, 64, 6, True),      # lane-per-row path, per-chunk activations
     ("t2", 2, 2048, 768, 128, 8, False),      # full geometry, two tokens
+    ("rows_t6", 6, 1024, 512, 32, 3, False),  # lane-per-row path, all tokens staged at once
+    ("rows_t21", 21, 512, 768, 16, 4, True),  # lane-per-row path, ragged 8-pair chunks, 12-warp down
 ]
 
 
