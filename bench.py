@@ -395,17 +395,19 @@ def run_ours(args, ws, rank, local):
 
     # per-kernel pass: events around the expert FFN (gate/up + down) on the launch stream
     with torch.cuda.stream(stream):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         torch.cuda.synchronize()
         for i in range(args.steps):
             r = i % R
+            evs[i][2].record(stream)
             g_rb[r].replay()
             evs[i][0].record(stream)
             g_ffn[r].replay()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
-    ffn_ms = [a.elapsed_time(b) for a, b in evs]
+    ffn_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    rb_ms = float(np.mean([c.elapsed_time(a) for a, _, c in evs]))
     ffn_ms_mean = float(np.mean(ffn_ms))
     ffn_alg = float(np.mean([ffn_bytes[i % R] for i in range(args.steps)]))
     peaks = load_peaks()
@@ -474,6 +476,7 @@ def run_ours(args, ws, rank, local):
             "data": "synthetic (seeded, qwen3_moe geometry, random-init Q8_0)",
             "config": workload_config(wl, args),
             "layer_hbm_gbs": layer_gbs, "near_ties": None,
+            "separate_path_ms": {"route_and_bucket": rb_ms, "expert_ffn": ffn_ms_mean},
             "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
             "gpu_launches": launches, "gpu_launches_source": launches_src, "clocks": clocks,
         }

@@ -301,6 +301,130 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_mask_kernel(const int32
     if (tid == 0 && s_bad) flag_status(status, MOE_STATUS_BAD_INDEX);
 }
 
+// Large batches over many CTAs, no inter-CTA communication: CTA c owns the
+// tokens of pair tile c (kTilePairs pairs).  Every CTA reads all the ids
+// (a few tens of KB, from L2) to count, per expert, all kept pairs and the
+// kept pairs of earlier tiles; it scans the totals into offsets itself and
+// ranks its own pairs with per-expert bitmaps of its tile.  A pair's position
+// is offsets[e] + (pairs of e in earlier tiles) + (its rank in the tile), the
+// same stable (token, slot) order as the single-CTA kernels.
+constexpr int kTilePairs = 1024;
+constexpr int kTileWords = kTilePairs / 32;
+
+__global__ void __launch_bounds__(kBucketThreads) bucket_tiles_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                                      int E, int32_t* __restrict__ offsets,
+                                                                      int32_t* __restrict__ pair_tok,
+                                                                      int32_t* __restrict__ pair_slot,
+                                                                      int32_t* __restrict__ pos, int32_t* status) {
+    __shared__ int s_total[MOE_MAX_EXPERTS], s_before[MOE_MAX_EXPERTS];
+    __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+    __shared__ int s_wsum[kBucketWarps];
+    __shared__ int s_bad;
+    extern __shared__ uint32_t bucket_dyn[];
+    uint32_t* s_mask = bucket_dyn;                                   // [E][kTileWords], bit = pair - tile start
+    int* s_pre = reinterpret_cast<int*>(bucket_dyn + E * kTileWords);  // [E][kTileWords] pairs in earlier words
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tpt = kTilePairs / k;  // tokens per tile
+    const int t0 = blockIdx.x * tpt, t1 = min(T, t0 + tpt);
+    pdl_wait();  // idx written by the router
+    pdl_launch_dependents();
+    for (int i = tid; i < E * kTileWords; i += kBucketThreads) s_mask[i] = 0;
+    if (tid < MOE_MAX_EXPERTS) {
+        s_total[tid] = 0;
+        s_before[tid] = 0;
+    }
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // 1. every token: validate, drop repeats; count; set this tile's bits
+    for (int t = tid; t < T; t += kBucketThreads) {
+        uint32_t seen[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) seen[j] = 0;
+        int ids[MOE_MAX_TOPK];
+#pragma unroll
+        for (int s2 = 0; s2 < MOE_MAX_TOPK; ++s2) ids[s2] = s2 < k ? __ldcg(idx + (size_t)t * k + s2) : -1;
+#pragma unroll
+        for (int s2 = 0; s2 < MOE_MAX_TOPK; ++s2) {
+            if (s2 >= k) break;
+            const int e = ids[s2];
+            bool ok = e >= 0 && e < E;
+            if (ok) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                    if (j == (e >> 5)) word = seen[j];
+                ok = !(word & (1u << (e & 31)));
+#pragma unroll
+                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                    if (j == (e >> 5)) seen[j] |= 1u << (e & 31);
+            }
+            if (!ok) {
+                s_bad = 1;
+                continue;
+            }
+            atomicAdd(&s_total[e], 1);
+            if (t < t0) {
+                atomicAdd(&s_before[e], 1);
+            } else if (t < t1) {
+                const int q = (t - t0) * k + s2;
+                atomicOr(&s_mask[e * kTileWords + (q >> 5)], 1u << (q & 31));
+            }
+        }
+    }
+    __syncthreads();
+    // 2. offsets (exclusive scan of the totals) and the tile's word prefixes
+    if (tid < MOE_MAX_EXPERTS) {
+        const int v = tid < E ? s_total[tid] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        s_off[tid] = incl - v;
+    }
+    for (int e = warp; e < E; e += kBucketWarps) {  // kTileWords == 32: one word per lane
+        const int c = __popc(s_mask[e * kTileWords + lane]);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        s_pre[e * kTileWords + lane] = incl - c;
+    }
+    __syncthreads();
+    if (tid < MOE_MAX_EXPERTS) {
+        int add = 0;
+        for (int w = 0; w < (tid >> 5); ++w) add += s_wsum[w];
+        if (tid < E) s_off[tid] += add;
+        if (tid == E - 1) s_off[E] = s_off[tid] + s_total[tid];
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int e = tid; e <= E; e += kBucketThreads) offsets[e] = s_off[e];
+    // 3. this tile's pairs
+    const int np = (t1 - t0) * k;
+    for (int q = tid; q < np; q += kBucketThreads) {
+        const int p = t0 * k + q;
+        const int e = __ldcg(idx + p);
+        int ps = -1;
+        if (e >= 0 && e < E) {
+            const uint32_t m = s_mask[e * kTileWords + (q >> 5)];
+            if (m & (1u << (q & 31)))
+                ps = s_off[e] + s_before[e] + s_pre[e * kTileWords + (q >> 5)] + __popc(m & ((1u << (q & 31)) - 1u));
+        }
+        pos[p] = ps;
+        if (ps >= 0) {
+            pair_tok[ps] = p / k;
+            pair_slot[ps] = p - (p / k) * k;
+        }
+    }
+    if (blockIdx.x == 0 && tid == 0 && s_bad) flag_status(status, MOE_STATUS_BAD_INDEX);
+}
+
 size_t bucket_mask_smem(int T, int k, int E) {
     const size_t W = ((size_t)T * k + 31) / 32;
     return (size_t)E * W * (sizeof(uint32_t) + sizeof(uint16_t));
@@ -312,14 +436,20 @@ constexpr size_t kBucketMaskCap = 200 * 1024;
 
 cudaError_t launch_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* pair_tok,
                           int32_t* pair_slot, int32_t* pos, int32_t* status, cudaStream_t s) {
+    const long long P = (long long)T * k;
     const size_t msmem = bucket_mask_smem(T, k, E);
-    const bool use_mask = (size_t)T * k <= 65535 && msmem <= kBucketMaskCap;  // word prefixes fit 16 bits
-    const size_t smem = use_mask ? msmem : (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t);
-    auto kern = use_mask ? bucket_mask_kernel : bucket_kernel;
+    // 2048+ pairs: tiles of 1024 pairs on as many CTAs (every CTA re-reads all
+    // ids, so very large batches keep the single-CTA kernels)
+    const bool use_tiles = P >= 2048 && T <= 16384;
+    const bool use_mask = !use_tiles && P <= 65535 && msmem <= kBucketMaskCap;  // word prefixes fit 16 bits
+    const size_t tsmem = (size_t)E * kTileWords * 2 * sizeof(uint32_t);
+    const size_t smem = use_tiles ? tsmem
+                                  : (use_mask ? msmem : (size_t)2 * kBucketWarps * ((E + 31) & ~31) * sizeof(uint32_t));
+    auto kern = use_tiles ? bucket_tiles_kernel : (use_mask ? bucket_mask_kernel : bucket_kernel);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
+    cfg.gridDim = dim3(use_tiles ? (unsigned)((T + kTilePairs / k - 1) / (kTilePairs / k)) : 1u, 1, 1);
     cfg.blockDim = dim3(kBucketThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

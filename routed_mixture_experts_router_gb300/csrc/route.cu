@@ -223,22 +223,28 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     const int kbeg = c * kslice;
     const int nch = kslice / kGemmKc;
 
-    // loaders: x chunk [32 tok][32 k] -> xs[k][tok]; Wr chunk [EP][32 k] -> ws[k][e]
-    const int lt = tid & 31, lk4 = tid >> 5;  // x: token lt, k quad lk4 (0..7)
+    // Loaders, coalesced: 8 lanes read one 128-byte row segment (token or
+    // expert row, 32 k), so a warp reads 4 whole segments per instruction.
+    // The chunks are stored transposed (xs[k][token], ws[k][expert]) with the
+    // 16-byte groups of a k row XOR-rotated by k/4: the transposing stores and
+    // the float4 reads of the FMA loop are both free of bank conflicts.
+    const int lr = tid >> 3, lq = tid & 7;  // row within the chunk, k quad
     float4 xr = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 wr[EPT];
     auto load = [&](int ch) {
         const int kk = kbeg + ch * kGemmKc;
-        const int t = t0 + lt;
-        xr = (t < T) ? __ldcg(reinterpret_cast<const float4*>(x + (size_t)t * dm + kk) + lk4)
+        const int t = t0 + lr;
+        xr = (t < T) ? __ldcg(reinterpret_cast<const float4*>(x + (size_t)t * dm + kk) + lq)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
-            const int e = (tid & 31) + 32 * j;  // expert row, k quad = tid >> 5
-            const float4* src = reinterpret_cast<const float4*>(Wr + (size_t)e * dm + kk) + (tid >> 5);
+            const int e = lr + 32 * j;
+            const float4* src = reinterpret_cast<const float4*>(Wr + (size_t)e * dm + kk) + lq;
             wr[j] = (e < E) ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
+    // column `col` of k row `kr` lives at swz(col, kr)
+    auto swz = [](int col, int kr) { return (((col >> 2) ^ ((kr >> 2) & 7)) << 2) | (col & 3); };
     pdl_wait();  // x is written by earlier kernels
     load(0);
     float acc[4][EPT];
@@ -248,27 +254,28 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
         for (int j = 0; j < EPT; ++j) acc[i][j] = 0.f;
     for (int ch = 0; ch < nch; ++ch) {
         __syncthreads();  // previous chunk consumed
-        xs[lk4 * 4 + 0][lt] = xr.x;
-        xs[lk4 * 4 + 1][lt] = xr.y;
-        xs[lk4 * 4 + 2][lt] = xr.z;
-        xs[lk4 * 4 + 3][lt] = xr.w;
+        {
+            const float xv4[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[lq * 4 + i][swz(lr, lq * 4 + i)] = xv4[i];
+        }
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
-            const int e = (tid & 31) + 32 * j, kq = tid >> 5;
-            ws[kq * 4 + 0][e] = wr[j].x;
-            ws[kq * 4 + 1][e] = wr[j].y;
-            ws[kq * 4 + 2][e] = wr[j].z;
-            ws[kq * 4 + 3][e] = wr[j].w;
+            const int e = lr + 32 * j;
+            const float wv4[4] = {wr[j].x, wr[j].y, wr[j].z, wr[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ws[lq * 4 + i][swz(e, lq * 4 + i)] = wv4[i];
         }
         __syncthreads();
         if (ch + 1 < nch) load(ch + 1);  // next chunk in flight during the FMAs
 #pragma unroll 8
         for (int kk = 0; kk < kGemmKc; ++kk) {
-            const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][tg * 4]);
+            const int rot = (kk >> 2) & 7;
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][(tg ^ rot) << 2]);
             float wv[EPT];
 #pragma unroll
             for (int j = 0; j < EPT; j += 4) {
-                const float4 q = *reinterpret_cast<const float4*>(&ws[kk][eg * EPT + j]);
+                const float4 q = *reinterpret_cast<const float4*>(&ws[kk][((eg * EPT + j) >> 2 ^ rot) << 2]);
                 wv[j] = q.x;
                 wv[j + 1] = q.y;
                 wv[j + 2] = q.z;

@@ -93,6 +93,44 @@ def test_bucket_skew_and_empty():
     check_bucket(idx, E, off.cpu().numpy(), pt.cpu().numpy(), ps.cpu().numpy(), pos.cpu().numpy())
 
 
+def test_bucket_bad_ids_many_tiles():
+    """Thousands of pairs (the many-CTA bucketing), odd k, invalid and repeated
+    ids: a pair is dropped (pos -1) when its id is out of range or repeats an
+    earlier slot of the same token; the rest are grouped by expert, stable in
+    (token, slot) order."""
+    T, k, E = 2100, 3, 64
+    rng = np.random.default_rng(5)
+    idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    bad = rng.random((T, k))
+    idx[bad < 0.01] = -1
+    idx[(bad >= 0.01) & (bad < 0.02)] = E + 7
+    idx[::97, 2] = idx[::97, 0]                 # repeats within a token
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    off, pt, ps, pos = binding.bucket(torch.from_numpy(idx).cuda(), E, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & binding.MOE_STATUS_BAD_INDEX
+    keep = np.zeros((T, k), dtype=bool)
+    for t in range(T):
+        seen = set()
+        for s in range(k):
+            e = int(idx[t, s])
+            if 0 <= e < E and e not in seen:
+                keep[t, s] = True
+            if 0 <= e < E:
+                seen.add(e)
+    pairs = [(int(idx[t, s]), t, s) for t in range(T) for s in range(k) if keep[t, s]]
+    pairs.sort()
+    exp_off = np.searchsorted(np.array([p[0] for p in pairs]), np.arange(E + 1), side="left")
+    exp_pos = -np.ones(T * k, dtype=np.int64)
+    for r, (_, t, s) in enumerate(pairs):
+        exp_pos[t * k + s] = r
+    assert np.array_equal(off.cpu().numpy(), exp_off)
+    assert np.array_equal(pos.cpu().numpy(), exp_pos)
+    n = len(pairs)
+    assert np.array_equal(pt.cpu().numpy()[:n], [p[1] for p in pairs])
+    assert np.array_equal(ps.cpu().numpy()[:n], [p[2] for p in pairs])
+
+
 def test_bucket_bad_ids_flag_status():
     idx = torch.tensor([[0, 1], [5, 5], [2, 99], [-1, 3]], dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -77,7 +77,7 @@ def test_tc_many_tokens_one_expert():
     _check(case)
 
 
-@pytest.mark.parametrize("name", ["prefill_t1024", "prefill_t768"])
+@pytest.mark.parametrize("name", ["prefill_t1024", "prefill_t768", "prefill_t2048"])
 def test_tc_prefill_full_sampled(name):
     """qwen3_moe geometry: routing for all tokens, outputs on sampled tokens."""
     case = make_case(synth.WORKLOADS[name])
