@@ -62,6 +62,11 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_rate(steps: int, units_per_step: int, ws: int, max_ms: float) -> float:
+    """Whole-job throughput: units every rank processed / the slowest rank's time."""
+    return steps * units_per_step * ws / (max_ms / 1e3)
+
+
 def max_over_ranks(v: float, ws: int, device) -> float:
     """Max of a host float over all ranks (timing only, not a data path)."""
     if ws == 1:
@@ -375,7 +380,7 @@ def run_ours(args, ws, rank, local):
     clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
     ms = max_over_ranks(ms_local, ws, dev)
     tokens = args.steps * wl.T * ws
-    value = tokens / (ms / 1e3)
+    value = job_rate(args.steps, wl.T, ws, ms)
 
     # One kernel node per step means the whole layer ran as the fused
     # single-launch decode kernel: that kernel is the roofline subject, timed
@@ -555,7 +560,7 @@ def run_stack(args, ws, rank, local):
     clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
     ms = max_over_ranks(ms_local, ws, dev)
     tokens = args.steps * wl.T * ws
-    value = tokens / (ms / 1e3)
+    value = job_rate(args.steps, wl.T, ws, ms)
 
     # dominant kernel: the expert FFN of each layer, timed alone (routing first, outside the events)
     P = wl.T * wl.k
