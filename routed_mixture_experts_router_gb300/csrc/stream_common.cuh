@@ -36,31 +36,41 @@ __device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
     return r;
 }
 
-// One word of four int8 -> (q0, q1), (q2, q3) as exact fp32 pairs.
-__device__ __forceinline__ void i8x4_to_f2(uint32_t w, f32x2& lo, f32x2& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const f32x2 bias = 0xCB000080CB000080ull;  // (-(2^23 + 128), -(2^23 + 128))
-    lo = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                        __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
-                bias);
-    hi = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                        __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
-                bias);
-}
-
-// sum over 16 values of q * x: one 16-byte weight chunk, four float4 of x at stride `st`.
-__device__ __forceinline__ float chunk_dot(const uint4 q, const float4* xv4, int st) {
-    f32x2 acc = 0ull;
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// The 16 weights of a chunk times their block scale d, exactly, as 8 fp32
+// pairs.  Byte u = q + 128 goes into the mantissa of 2^15 (v = 2^15 + u), and
+// fma(v, d, -(2^15 + 128) d) = q d: the constant is exact (9 x 11 significant
+// bits) and so is the result (q d has at most 19), so the one rounding of
+// the fma changes nothing.
+__device__ __forceinline__ void dequant16(const uint4 q, float d, f32x2 (&w)[8]) {
+    const f32x2 dd = f2_pack(d, d);
+    const float c = -32896.0f * d;
+    const f32x2 cc = f2_pack(c, c);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        f32x2 lo, hi;
-        i8x4_to_f2(w[m], lo, hi);
-        const float4 xv = xv4[m * st];
-        acc = f2_fma(lo, f2_pack(xv.x, xv.y), acc);
-        acc = f2_fma(hi, f2_pack(xv.z, xv.w), acc);
+        const uint32_t u = words[m] ^ 0x80808080u;
+        w[2 * m] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
+                                  __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
+                          dd, cc);
+        w[2 * m + 1] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7524)),
+                                      __uint_as_float(__byte_perm(u, 0x47000000u, 0x7534))),
+                              dd, cc);
     }
-    return f2_sum(acc);
+}
+
+// sum over 16 values of (q * d) * x: one 16-byte weight chunk dequantised
+// with its block scale d (exactly), four float4 of x at stride `st`.
+__device__ __forceinline__ float chunk_dot_scaled(const uint4 q, float d, const float4* xv4, int st) {
+    f32x2 w[8];
+    dequant16(q, d, w);
+    f32x2 acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 xv = xv4[m * st];
+        acc0 = f2_fma(w[2 * m], f2_pack(xv.x, xv.y), acc0);
+        acc1 = f2_fma(w[2 * m + 1], f2_pack(xv.z, xv.w), acc1);
+    }
+    return f2_sum(f2_add(acc0, acc1));
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -225,8 +235,8 @@ __device__ __forceinline__ void gu_compute_item(const unsigned char* b, int r, i
                 for (int g2 = 0; g2 < G; ++g2) {
                     if (g2 < ng) {
                         const float4* xv = xs + toff[g2] + m * 4 * 32 + lane;
-                        ga[g2] = fmaf(sg, chunk_dot(qg, xv, 32), ga[g2]);
-                        ua[g2] = fmaf(su, chunk_dot(qu, xv, 32), ua[g2]);
+                        ga[g2] += chunk_dot_scaled(qg, sg, xv, 32);
+                        ua[g2] += chunk_dot_scaled(qu, su, xv, 32);
                     }
                 }
             }
@@ -288,7 +298,7 @@ __device__ __forceinline__ void dn_compute_item(const unsigned char* b, int qd, 
 #pragma unroll
                     for (int g2 = 0; g2 < G; ++g2)
                         if (g2 < ng)
-                            acc[rr][g2] = fmaf(s, chunk_dot(q, hs + hoff[g2] + m * 4 * LPR + hl, LPR), acc[rr][g2]);
+                            acc[rr][g2] += chunk_dot_scaled(q, s, hs + hoff[g2] + m * 4 * LPR + hl, LPR);
                 }
             }
         }
@@ -329,28 +339,6 @@ __device__ __forceinline__ void dn_compute_item(const unsigned char* b, int qd, 
 // and reused for every token of the item; the per-token partial sums are
 // reduced across lanes with one butterfly reduce-scatter.
 constexpr int kMultiG = 8;
-
-// The 16 weights of a chunk times their block scale d, exactly, as 8 fp32
-// pairs.  Byte u = q + 128 goes into the mantissa of 2^15 (v = 2^15 + u), and
-// fma(v, d, -(2^15 + 128) d) = q d: the constant is exact (9 x 11 significant
-// bits) and so is the result (q d has at most 19), so the one rounding of
-// the fma changes nothing.
-__device__ __forceinline__ void dequant16(const uint4 q, float d, f32x2 (&w)[8]) {
-    const f32x2 dd = f2_pack(d, d);
-    const float c = -32896.0f * d;
-    const f32x2 cc = f2_pack(c, c);
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const uint32_t u = words[m] ^ 0x80808080u;
-        w[2 * m] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
-                                  __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
-                          dd, cc);
-        w[2 * m + 1] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7524)),
-                                      __uint_as_float(__byte_perm(u, 0x47000000u, 0x7534))),
-                              dd, cc);
-    }
-}
 
 // One reduce-scatter step over lane pairs (L, L ^ o): N values in, N/2 out.
 // The lane with (L & o) set keeps the upper half.  After steps o = W/2, ...,
