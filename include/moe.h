@@ -69,10 +69,14 @@ extern "C" {
 
 /* ---- device status bits (OR-ed into *status) ------------------------- */
 #define MOE_STATUS_BAD_INDEX 1 /* an expert id outside [0, E), or repeated in one token */
+#define MOE_STATUS_TIMEOUT 2   /* a bounded on-device wait (grid barrier, mbarrier) gave up after
+                                  2 s; that call's outputs are invalid */
 
 /* ---- expert-input precision ------------------------------------------ */
 #define MOE_ACT_F32 0  /* fp32 activations, CUDA-core Q8_0 contraction (decode) */
-#define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill) */
+#define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill); batches
+                          of fewer than 128 pairs, or dimensions not multiples of 128, run the
+                          fp32 path (more accurate, and memory-bound at that size anyway) */
 
 /* ---- flags ----------------------------------------------------------- */
 #define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */
@@ -141,7 +145,10 @@ MOE_API int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets
  * Expert SwiGLU FFNs over the bucketed pairs, Q8_0 dequantisation fused into
  * the contractions.
  *   x: fp32 [T][d_model] expert inputs (token-indexed)
- *   offsets, pair_tok, pair_slot, pos, wts: from moe_bucket / moe_route
+ *   offsets, pair_tok, pair_slot, pos, wts: from moe_bucket / moe_route.
+ *       Every bucket is clamped into [0, T*k] and token / slot ids are
+ *       range-checked, so offsets that are not a valid bucketing give wrong
+ *       values but no access outside the arrays.
  *   act: MOE_ACT_F32 (fp32 FMA) or MOE_ACT_BF16 (tcgen05, bf16 operands,
  *        fp32 accumulation)
  *   fuse_combine = 1: out_or_ypairs is out fp32 [T][d_model]; it is
@@ -167,7 +174,17 @@ MOE_API int moe_combine(const float* ypairs, const float* wts, const int32_t* po
 
 /*
  * The whole layer: route -> bucket -> gate/up -> down + combine.
- *   x: fp32 [T][d_model]; out: fp32 [T][d_model], must not alias x
+ *   x: fp32 [T][d_model]; out: fp32 [T][d_model], must not alias x.
+ *       x is only read, with plain loads, so it may also be a page-locked
+ *       host buffer the GPU addresses directly (on GB300 the host memory is
+ *       coherent with the GPU over NVLink-C2C); that pays off only for a
+ *       token or two, where it saves a separate copy.
+ * Paths: one or two tokens on the fp32 path without MOE_FLAG_DETERMINISTIC
+ * run as ONE cooperative kernel (router, top-k, bucketing, gate/up, down and
+ * combine; an 8-byte memset of the workspace's barrier words precedes it);
+ * otherwise router, bucketing and the expert kernels (tcgen05 for MOE_ACT_BF16
+ * with >= 128 pairs).  Grid barriers and mbarrier waits are bounded
+ * (MOE_STATUS_TIMEOUT).
  *   act: MOE_ACT_F32 or MOE_ACT_BF16; flags: MOE_FLAG_*
  *   residual: 1 adds x to the output (a residual stream between layers)
  *   idx_out [T][k], wts_out [T][k], offsets_out [E+1]: optional copies of the

@@ -21,6 +21,7 @@ MOE_ERR_UNSUPPORTED = 2
 MOE_ERR_CUDA = 3
 MOE_ERR_WORKSPACE = 4
 MOE_STATUS_BAD_INDEX = 1
+MOE_STATUS_TIMEOUT = 2
 MOE_ACT_F32 = 0
 MOE_ACT_BF16 = 1
 MOE_FLAG_DETERMINISTIC = 1

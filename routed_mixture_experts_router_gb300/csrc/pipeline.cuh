@@ -5,9 +5,11 @@
 
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
 
-constexpr int MOE_STATUS_TIMEOUT_BIT = 2;
+constexpr int MOE_STATUS_TIMEOUT_BIT = MOE_STATUS_TIMEOUT;
 constexpr unsigned long long kWaitDeadlineNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
