@@ -8,8 +8,9 @@ never imports the product: the two share only the seeded input generators.
 The arithmetic lives in ``moe_oracle.c`` (plain C, fp64, no CUDA headers),
 compiled with gcc into ``oracle/_build/liboracle.so`` and called via ctypes.
 Every function takes and returns numpy arrays.  Weights are Q8_0 in the pages'
-own 34-byte block format (fp16 scale, then 32 int8 values along K), as raw
-uint8 arrays; the oracle decodes them itself.
+own 34-byte block format (fp16 scale, then 32 int8 values along K) or Q4_0
+(18-byte blocks: fp16 scale, 16 bytes of 4-bit values), as raw uint8 arrays;
+the oracle decodes them itself.
 """
 from __future__ import annotations
 
@@ -66,6 +67,11 @@ class Oracle:
         lib.oracle_route.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
         lib.oracle_moe_layer.restype = _I
         lib.oracle_moe_layer.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]
+        lib.oracle_moe_layer_fmt.restype = _I
+        lib.oracle_moe_layer_fmt.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
+                                             _P, _P]
+        lib.oracle_dequant.restype = None
+        lib.oracle_dequant.argtypes = [_P, _I, _I, _I, _P]
         lib.oracle_bucket.restype = _I
         lib.oracle_bucket.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P]
         lib.oracle_q8_block_bytes.restype = _I
@@ -102,6 +108,14 @@ class Oracle:
         self.lib.oracle_dequant_q8(self._p(b), rows, K, self._p(out))
         return out
 
+    def dequant(self, blocks: np.ndarray, rows: int, K: int, fmt: int) -> np.ndarray:
+        """fmt 0: Q8_0 (34-byte blocks); 1: Q4_0 (18-byte blocks)."""
+        b = self._c(blocks, np.uint8)
+        assert b.size == rows * (K // 32) * (18 if fmt == 1 else 34)
+        out = np.empty((rows, K), dtype=np.float64)
+        self.lib.oracle_dequant(self._p(b), rows, K, fmt, self._p(out))
+        return out
+
     def expert_swiglu(self, gate, up, down, dm: int, f: int, x: np.ndarray) -> np.ndarray:
         g, u, d = (self._c(a, np.uint8) for a in (gate, up, down))
         xv = self._c(x, np.float64)
@@ -125,8 +139,9 @@ class Oracle:
         return idx, w, logits
 
     def moe_layer(self, x, Wr, bias, gate, up, down, dm: int, f: int, E: int, k: int, residual: bool = False,
-                  expert_input_bf16: bool = False, forced_idx=None):
-        """Returns (out [T][dm] f64, idx [T][k] i32, w [T][k] f64, logits [T][E] f64)."""
+                  expert_input_bf16: bool = False, forced_idx=None, fmt: int = 0):
+        """Returns (out [T][dm] f64, idx [T][k] i32, w [T][k] f64, logits [T][E] f64).
+        fmt: expert block format, 0 = Q8_0, 1 = Q4_0."""
         xv = self._c(x, np.float64).reshape(-1, dm)
         T = xv.shape[0]
         wr = self._c(Wr, np.float32)
@@ -137,9 +152,9 @@ class Oracle:
         idx = np.empty((T, k), dtype=np.int32)
         w = np.empty((T, k), dtype=np.float64)
         logits = np.empty((T, E), dtype=np.float64)
-        rc = self.lib.oracle_moe_layer(T, dm, f, E, k, self._p(xv), self._p(wr), self._p(b), self._p(g), self._p(u),
-                                       self._p(d), int(residual), int(expert_input_bf16), self._p(fi), self._p(out),
-                                       self._p(idx), self._p(w), self._p(logits))
+        rc = self.lib.oracle_moe_layer_fmt(T, dm, f, E, k, self._p(xv), self._p(wr), self._p(b), self._p(g),
+                                           self._p(u), self._p(d), int(fmt), int(residual), int(expert_input_bf16),
+                                           self._p(fi), self._p(out), self._p(idx), self._p(w), self._p(logits))
         if rc != 0:
             raise ValueError(f"oracle_moe_layer rc={rc}")
         return out, idx, w, logits

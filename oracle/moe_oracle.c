@@ -37,6 +37,13 @@
  * Q8_0 block (34 bytes, little endian): fp16 scale d, then 32 int8 values q
  * along K.  A Q8_0 matrix of rows x K is rows * (K/32) blocks, row-major.
  *
+ * Q4_0 block (18 bytes): fp16 scale d, then 16 bytes holding 32 unsigned
+ * 4-bit values n along K: byte j carries element j in its low nibble and
+ * element j + 16 in its high nibble; w = (n - 8) * d.  ("Q4 expert
+ * execution", amalgafy.com/technical-overview, "Execution architecture"; the
+ * pages give no block layout, so this is the plain 4-bit sibling of Q8_0:
+ * same 32-wide blocks and fp16 scale, values offset by 8.)
+ *
  * Parallelism: tokens are independent, so the token loops may run under
  * OpenMP; that changes no arithmetic and no summation order.
  */
@@ -92,17 +99,48 @@ static void dequant_row(const uint8_t* row_blocks, int K, double* w) {
     }
 }
 
-/* Dequantise a whole rows x K Q8_0 matrix into out[rows][K]. */
-void oracle_dequant_q8(const uint8_t* blocks, int rows, int K, double* out) {
-    size_t row_bytes = (size_t)(K / ORACLE_Q8_BLOCK_ELEMS) * ORACLE_Q8_BLOCK_BYTES;
-    for (int r = 0; r < rows; ++r) dequant_row(blocks + (size_t)r * row_bytes, K, out + (size_t)r * K);
+#define ORACLE_Q4_BLOCK_BYTES 18
+
+/* Dequantise one Q4_0 row of K weights: w = (n - 8) * d. */
+static void dequant_row_q4(const uint8_t* row_blocks, int K, double* w) {
+    int nb = K / ORACLE_Q8_BLOCK_ELEMS;
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t* q4b = row_blocks + (size_t)b * ORACLE_Q4_BLOCK_BYTES;
+        double d4 = oracle_half_to_double((uint16_t)(q4b[0] | (q4b[1] << 8)));
+        for (int j = 0; j < 16; ++j) {
+            int lo = q4b[2 + j] & 0x0F, hi = q4b[2 + j] >> 4;
+            w[b * ORACLE_Q8_BLOCK_ELEMS + j] = (double)(lo - 8) * d4;
+            w[b * ORACLE_Q8_BLOCK_ELEMS + 16 + j] = (double)(hi - 8) * d4;
+        }
+    }
 }
 
-/* y[r] = sum_j W[r][j] * v[j], W given as Q8_0 rows x K, j ascending. */
-static void q8_matvec(const uint8_t* blocks, int rows, int K, const double* v, double* y, double* wrow) {
-    size_t row_bytes = (size_t)(K / ORACLE_Q8_BLOCK_ELEMS) * ORACLE_Q8_BLOCK_BYTES;
+/* Block format: 0 = Q8_0, 1 = Q4_0. */
+static size_t row_bytes_of(int K, int fmt) {
+    return (size_t)(K / ORACLE_Q8_BLOCK_ELEMS) * (fmt == 1 ? ORACLE_Q4_BLOCK_BYTES : ORACLE_Q8_BLOCK_BYTES);
+}
+
+static void dequant_row_fmt(const uint8_t* row_blocks, int K, int fmt, double* w) {
+    if (fmt == 1)
+        dequant_row_q4(row_blocks, K, w);
+    else
+        dequant_row(row_blocks, K, w);
+}
+
+/* Dequantise a whole rows x K matrix (format fmt) into out[rows][K]. */
+void oracle_dequant(const uint8_t* blocks, int rows, int K, int fmt, double* out) {
+    size_t row_bytes = row_bytes_of(K, fmt);
+    for (int r = 0; r < rows; ++r) dequant_row_fmt(blocks + (size_t)r * row_bytes, K, fmt, out + (size_t)r * K);
+}
+
+/* Dequantise a whole rows x K Q8_0 matrix into out[rows][K]. */
+void oracle_dequant_q8(const uint8_t* blocks, int rows, int K, double* out) { oracle_dequant(blocks, rows, K, 0, out); }
+
+/* y[r] = sum_j W[r][j] * v[j], W given as rows x K blocks of format fmt, j ascending. */
+static void q_matvec(const uint8_t* blocks, int rows, int K, int fmt, const double* v, double* y, double* wrow) {
+    size_t row_bytes = row_bytes_of(K, fmt);
     for (int r = 0; r < rows; ++r) {
-        dequant_row(blocks + (size_t)r * row_bytes, K, wrow);
+        dequant_row_fmt(blocks + (size_t)r * row_bytes, K, fmt, wrow);
         double acc = 0.0;
         for (int j = 0; j < K; ++j) acc += wrow[j] * v[j];
         y[r] = acc;
@@ -113,21 +151,26 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /*
  * One SwiGLU expert on one token vector.
- *   gate, up: Q8_0 [f][dm] (K = dm); down: Q8_0 [dm][f] (K = f).
+ *   gate, up: [f][dm] (K = dm); down: [dm][f] (K = f); blocks of format fmt.
  *   x[dm] -> y[dm].
  */
-void oracle_expert_swiglu(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f,
-                          const double* x, double* y) {
+void oracle_expert_swiglu_fmt(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f, int fmt,
+                              const double* x, double* y) {
     int kmax = dm > f ? dm : f;
     double* g = (double*)malloc(sizeof(double) * (size_t)f);
     double* u = (double*)malloc(sizeof(double) * (size_t)f);
     double* h = (double*)malloc(sizeof(double) * (size_t)f);
     double* wrow = (double*)malloc(sizeof(double) * (size_t)kmax);
-    q8_matvec(gate, f, dm, x, g, wrow);
-    q8_matvec(up, f, dm, x, u, wrow);
+    q_matvec(gate, f, dm, fmt, x, g, wrow);
+    q_matvec(up, f, dm, fmt, x, u, wrow);
     for (int r = 0; r < f; ++r) h[r] = silu(g[r]) * u[r];
-    q8_matvec(down, dm, f, h, y, wrow);
+    q_matvec(down, dm, f, fmt, h, y, wrow);
     free(g); free(u); free(h); free(wrow);
+}
+
+void oracle_expert_swiglu(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f,
+                          const double* x, double* y) {
+    oracle_expert_swiglu_fmt(gate, up, down, dm, f, 0, x, y);
 }
 
 /*
@@ -201,23 +244,25 @@ int oracle_route(int T, int dm, int E, int k, const double* x, const float* Wr, 
  * One MoE layer.
  *   x [T][dm] (fp64 values; the router reads them as given)
  *   Wr [E][dm] fp32, bias [E] fp32 or NULL
- *   gate, up: E experts of Q8_0 [f][dm]; down: E experts of Q8_0 [dm][f]
+ *   gate, up: E experts of [f][dm]; down: E experts of [dm][f]; blocks of
+ *       format fmt (0 = Q8_0, 1 = Q4_0)
  *   residual: add x[t] to the combined output
  *   expert_input_bf16: feed the experts bf16(fp32(x)) instead of x (the
  *       tensor-core path's cast; the router still reads x)
  *   forced_idx [T][k] or NULL: use this selection instead of the top-k
  *   out [T][dm]; idx [T][k]; w [T][k]; logits [T][E] or NULL
  */
-int oracle_moe_layer(int T, int dm, int f, int E, int k, const double* x, const float* Wr, const float* bias,
-                     const uint8_t* gate, const uint8_t* up, const uint8_t* down, int residual,
-                     int expert_input_bf16, const int32_t* forced_idx, double* out, int32_t* idx, double* w,
-                     double* logits) {
+int oracle_moe_layer_fmt(int T, int dm, int f, int E, int k, const double* x, const float* Wr, const float* bias,
+                         const uint8_t* gate, const uint8_t* up, const uint8_t* down, int fmt, int residual,
+                         int expert_input_bf16, const int32_t* forced_idx, double* out, int32_t* idx, double* w,
+                         double* logits) {
     if (T < 0 || dm <= 0 || f <= 0 || E <= 0 || k <= 0 || k > E) return -1;
     if (dm % ORACLE_Q8_BLOCK_ELEMS || f % ORACLE_Q8_BLOCK_ELEMS) return -1;
     if (T == 0) return 0;
     if (!x || !Wr || !gate || !up || !down || !out || !idx || !w) return -1;
-    size_t gu_bytes = (size_t)f * (dm / ORACLE_Q8_BLOCK_ELEMS) * ORACLE_Q8_BLOCK_BYTES;
-    size_t dn_bytes = (size_t)dm * (f / ORACLE_Q8_BLOCK_ELEMS) * ORACLE_Q8_BLOCK_BYTES;
+    if (fmt != 0 && fmt != 1) return -1;
+    size_t gu_bytes = (size_t)f * row_bytes_of(dm, fmt);
+    size_t dn_bytes = (size_t)dm * row_bytes_of(f, fmt);
     int bad = 0;
     int t;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
@@ -235,8 +280,8 @@ int oracle_moe_layer(int T, int dm, int f, int E, int k, const double* x, const 
         for (int s = 0; s < k; ++s) {
             int e = it[s];
             if (e < 0 || e >= E) { bad = 1; continue; }
-            oracle_expert_swiglu(gate + (size_t)e * gu_bytes, up + (size_t)e * gu_bytes,
-                                 down + (size_t)e * dn_bytes, dm, f, xin, y);
+            oracle_expert_swiglu_fmt(gate + (size_t)e * gu_bytes, up + (size_t)e * gu_bytes,
+                                     down + (size_t)e * dn_bytes, dm, f, fmt, xin, y);
             for (int o = 0; o < dm; ++o) acc[o] += wt[s] * y[o];
         }
         double* ot = out + (size_t)t * dm;
@@ -244,6 +289,15 @@ int oracle_moe_layer(int T, int dm, int f, int E, int k, const double* x, const 
         free(lg); free(xin); free(y); free(acc);
     }
     return bad ? -2 : 0;
+}
+
+/* The layer with Q8_0 experts. */
+int oracle_moe_layer(int T, int dm, int f, int E, int k, const double* x, const float* Wr, const float* bias,
+                     const uint8_t* gate, const uint8_t* up, const uint8_t* down, int residual,
+                     int expert_input_bf16, const int32_t* forced_idx, double* out, int32_t* idx, double* w,
+                     double* logits) {
+    return oracle_moe_layer_fmt(T, dm, f, E, k, x, Wr, bias, gate, up, down, 0, residual, expert_input_bf16,
+                                forced_idx, out, idx, w, logits);
 }
 
 /*

@@ -36,6 +36,7 @@ import torch
 
 Q8_BLOCK = 32
 Q8_BLOCK_BYTES = 34
+Q4_BLOCK_BYTES = 18
 
 # tensor ids for the seed scheme
 _T_X, _T_WR, _T_BIAS, _T_GATE, _T_UP, _T_DOWN = range(6)
@@ -55,6 +56,7 @@ class Workload:
     act: str = "f32"  # "f32": fp32 expert inputs; "bf16": tensor-core path
     layers: int = 1
     residual: bool = False
+    wfmt: str = "q8"  # expert weight blocks: "q8" (Q8_0, 34 B) or "q4" (Q4_0, 18 B)
 
 
 WORKLOADS = {
@@ -73,6 +75,9 @@ WORKLOADS = {
     "stack48_t64": Workload("stack48_t64", 5, 64, 2048, 768, 128, 8, zipf=True, layers=48, residual=True),
     "stack48_t1024": Workload("stack48_t1024", 5, 1024, 2048, 768, 128, 8, zipf=True, act="bf16", layers=48,
                               residual=True),
+    # Q4_0 experts (the 4-bit format of the pages' next stage), decode
+    "decode_t1_q4": Workload("decode_t1_q4", 6, 1, 2048, 768, 128, 8, wfmt="q4"),
+    "decode_t64_zipf_q4": Workload("decode_t64_zipf_q4", 7, 64, 2048, 768, 128, 8, zipf=True, wfmt="q4"),
 }
 
 
@@ -109,6 +114,35 @@ def quantize_q8_0(w: torch.Tensor) -> torch.Tensor:
     return by.reshape(*lead, (K // Q8_BLOCK) * Q8_BLOCK_BYTES).contiguous()
 
 
+def quantize_q4_0(w: torch.Tensor) -> torch.Tensor:
+    """Encode fp32 weights [..., K] (K % 32 == 0) into Q4_0 bytes [..., K/32*18] (uint8).
+
+    Per 32-block: d32 = max|w| / 7, q = clamp(round_half_away(w / d32), -8, 7),
+    stored as n = q + 8 in 4 bits: byte j holds element j (low nibble) and
+    element j + 16 (high nibble); the fp16 scale leads the block.
+    """
+    assert w.dtype == torch.float32 and w.shape[-1] % Q8_BLOCK == 0
+    lead = w.shape[:-1]
+    K = w.shape[-1]
+    blk = w.reshape(*lead, K // Q8_BLOCK, Q8_BLOCK)
+    amax = blk.abs().amax(dim=-1, keepdim=True)
+    d32 = amax / 7.0
+    safe = torch.where(d32 > 0, d32, torch.ones_like(d32))
+    v = blk / safe
+    q = torch.sign(v) * torch.floor(v.abs() + 0.5)
+    q = torch.clamp(q, -8, 7)
+    q = torch.where(d32 > 0, q, torch.zeros_like(q))
+    n = (q + 8).to(torch.uint8)
+    packed = n[..., :16] | (n[..., 16:] << 4)
+    d16 = d32.to(torch.float16)
+    by = torch.cat([d16.contiguous().view(torch.uint8), packed.contiguous()], dim=-1)
+    return by.reshape(*lead, (K // Q8_BLOCK) * Q4_BLOCK_BYTES).contiguous()
+
+
+def q4_matrix_bytes(rows: int, K: int) -> int:
+    return rows * (K // Q8_BLOCK) * Q4_BLOCK_BYTES
+
+
 def q8_matrix_bytes(rows: int, K: int) -> int:
     return rows * (K // Q8_BLOCK) * Q8_BLOCK_BYTES
 
@@ -139,26 +173,29 @@ def make_router(wl: Workload, layer: int, device):
 
 
 def make_expert_q8(wl: Workload, layer: int, which: str, device, chunk: int = 16) -> torch.Tensor:
-    """Q8_0 bytes of one expert matrix family for all E experts.
+    """Quantised bytes of one expert matrix family for all E experts, in the
+    workload's block format (Q8_0, or Q4_0 when wl.wfmt == "q4").
 
     which = "gate" | "up": E x [d_ff][d_model]; "down": E x [d_model][d_ff].
-    Returns uint8 [E][rows * K/32 * 34].  Generated `chunk` experts at a time
-    to bound temporary memory.
+    Returns uint8 [E][rows * K/32 * block bytes].  Generated `chunk` experts at
+    a time to bound temporary memory.
     """
     tid = {"gate": _T_GATE, "up": _T_UP, "down": _T_DOWN}[which]
     rows, K = (wl.d_ff, wl.d_model) if which != "down" else (wl.d_model, wl.d_ff)
+    q4 = wl.wfmt == "q4"
     g = _gen(device, seed_for(wl.wid, layer, tid))
-    out = torch.empty(wl.E, q8_matrix_bytes(rows, K), dtype=torch.uint8, device=device)
+    nbytes = q4_matrix_bytes(rows, K) if q4 else q8_matrix_bytes(rows, K)
+    out = torch.empty(wl.E, nbytes, dtype=torch.uint8, device=device)
     for e0 in range(0, wl.E, chunk):
         n = min(chunk, wl.E - e0)
         w = torch.randn(n, rows, K, generator=g, device=device, dtype=torch.float32).mul_(0.02)
-        out[e0:e0 + n] = quantize_q8_0(w).reshape(n, -1)
+        out[e0:e0 + n] = (quantize_q4_0(w) if q4 else quantize_q8_0(w)).reshape(n, -1)
         del w
     return out
 
 
 def make_layer(wl: Workload, layer: int, device) -> dict:
-    """All weights of one layer: Wr, bias, and Q8_0 gate/up/down bytes (AoS blocks)."""
+    """All weights of one layer: Wr, bias, and quantised gate/up/down bytes (AoS blocks)."""
     Wr, bias = make_router(wl, layer, device)
     return {
         "Wr": Wr,

@@ -32,18 +32,27 @@ def np_dequant(blocks: np.ndarray, rows: int, K: int) -> np.ndarray:
     return (q * d[:, None]).reshape(rows, K)
 
 
-def tiny_layer(seed: int, T: int, dm: int, f: int, E: int, k: int, zipf: bool = False):
-    wl = synth.custom(f"tiny{seed}", wid=1000 + seed, T=T, d_model=dm, d_ff=f, E=E, k=k, zipf=zipf)
+def np_dequant_q4(blocks: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Independent Q4_0 decode with numpy (fp64): nibbles split by array ops."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 18)
+    d = b[:, :2].copy().view("<f2").astype(np.float64)[:, 0]
+    p = b[:, 2:].astype(np.int64)
+    n = np.concatenate([p % 16, p // 16], axis=1)
+    return ((n - 8).astype(np.float64) * d[:, None]).reshape(rows, K)
+
+
+def tiny_layer(seed: int, T: int, dm: int, f: int, E: int, k: int, zipf: bool = False, wfmt: str = "q8"):
+    wl = synth.custom(f"tiny{seed}", wid=1000 + seed, T=T, d_model=dm, d_ff=f, E=E, k=k, zipf=zipf, wfmt=wfmt)
     w = synth.make_layer(wl, 0, "cpu")
     x = synth.make_x(wl, "cpu").double().numpy()
     return wl, x, {kk: (None if v is None else v.numpy()) for kk, v in w.items()}
 
 
-def dense_bruteforce(x, Wr, bias, gate, up, down, dm, f, E, k, residual=False):
+def dense_bruteforce(x, Wr, bias, gate, up, down, dm, f, E, k, residual=False, deq=np_dequant):
     """All E experts for every token, full softmax, mask to top-k, renormalise, sum."""
-    Wg = np.stack([np_dequant(gate[e], f, dm) for e in range(E)])
-    Wu = np.stack([np_dequant(up[e], f, dm) for e in range(E)])
-    Wd = np.stack([np_dequant(down[e], dm, f) for e in range(E)])
+    Wg = np.stack([deq(gate[e], f, dm) for e in range(E)])
+    Wu = np.stack([deq(up[e], f, dm) for e in range(E)])
+    Wd = np.stack([deq(down[e], dm, f) for e in range(E)])
     logits = x @ Wr.astype(np.float64).T
     if bias is not None:
         logits = logits + bias.astype(np.float64)[None, :]
@@ -252,6 +261,53 @@ def pin_residual_stack(orc):
     assert np.abs(a).max() > 0
 
 
+def pin_q4_block_layout(orc):
+    """Q4_0 reading, on hand-built blocks: the fp16 scale leads (little
+    endian), byte j's low nibble is element j and its high nibble element
+    j + 16, values are (n - 8) * d, blocks run along K and rows follow rows."""
+    a = bytes([0x00, 0x3C]) + bytes(j | ((15 - j) << 4) for j in range(16))    # d = 1.0
+    b = bytes([0x00, 0xB8]) + bytes([0x8F] * 16)                              # d = -0.5
+    blocks = np.frombuffer(a + b + b + a, dtype=np.uint8)                     # 2 rows x 64
+    got = orc.dequant(blocks, 2, 64, 1)
+    blk_a = [float(j - 8) for j in range(16)] + [float(7 - j) for j in range(16)]
+    blk_b = [-3.5] * 16 + [0.0] * 16
+    assert got.tolist() == [blk_a + blk_b, blk_b + blk_a], got
+    assert np.array_equal(got, np_dequant_q4(blocks, 2, 64))
+
+
+def pin_q4_roundtrip(orc):
+    """Q4_0: re-encoding the decoded weights gives the same bytes, every value
+    lies within half a step of the fp32 weight it encodes (plus the fp16
+    rounding of the scale), and the decode is exact in fp32."""
+    g = torch.Generator().manual_seed(11)
+    w = torch.randn(12, 128, generator=g) * 0.02
+    w[2, 32:64] = 0.0
+    blocks = synth.quantize_q4_0(w).numpy()
+    assert blocks.shape == (12, 4 * 18)
+    deq = orc.dequant(blocks, 12, 128, 1)
+    again = synth.quantize_q4_0(torch.from_numpy(deq.astype(np.float32))).numpy()
+    assert np.array_equal(again, blocks)
+    amax = w.reshape(12, 4, 32).abs().amax(-1).double().numpy()
+    step = np.repeat(amax / 7.0, 32, axis=1)
+    assert np.all(np.abs(deq - w.double().numpy()) <= 0.5 * step * (1 + 2e-3) + 1e-12)
+    assert np.all(deq[2, 32:64] == 0.0)
+    assert np.array_equal(deq.astype(np.float32).astype(np.float64), deq)
+
+
+def pin_dense_bruteforce_q4(orc):
+    """Sparse oracle with Q4_0 experts == dense brute force over all experts
+    decoded by numpy; the Q8_0 layer of the same seed differs from it."""
+    for seed, (T, dm, f, E, k, zipf) in enumerate([(4, 64, 32, 8, 2, False), (6, 96, 64, 12, 3, True)]):
+        wl, x, w = tiny_layer(40 + seed, T, dm, f, E, k, zipf, wfmt="q4")
+        assert w["gate"].shape == (E, f * dm // 32 * 18)
+        out, idx, wt, _ = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k, fmt=1)
+        ro, ridx, rw, _ = dense_bruteforce(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k,
+                                           deq=np_dequant_q4)
+        assert np.array_equal(idx, ridx)
+        assert np.allclose(wt, rw, rtol=1e-12, atol=1e-15)
+        assert rel_l2_max(out, ro) < 1e-12, rel_l2_max(out, ro)
+
+
 ALL_PINS = [
     pin_half_decode,
     pin_q8_roundtrip,
@@ -264,4 +320,7 @@ ALL_PINS = [
     pin_single_expert_swiglu,
     pin_bucket_bruteforce,
     pin_residual_stack,
+    pin_q4_block_layout,
+    pin_q4_roundtrip,
+    pin_dense_bruteforce_q4,
 ]

@@ -26,6 +26,14 @@ MUTANTS = {
     "bucket_unstable": ("int p = off[e] + cnt[e]++;", "int p = off[e + 1] - 1 - cnt[e]++;"),
     "combine_slot_shift": ("int e = it[s];", "int e = it[(s + 1) % k];"),
     "block_stride": ("#define ORACLE_Q8_BLOCK_BYTES 34", "#define ORACLE_Q8_BLOCK_BYTES 36"),
+    "q4_nibble_swap": ("int lo = q4b[2 + j] & 0x0F, hi = q4b[2 + j] >> 4;",
+                       "int hi = q4b[2 + j] & 0x0F, lo = q4b[2 + j] >> 4;"),
+    "q4_offset": ("(double)(hi - 8) * d4", "(double)(hi - 7) * d4"),
+    "q4_interleaved": ("w[b * ORACLE_Q8_BLOCK_ELEMS + j] = (double)(lo - 8) * d4;\n"
+                       "            w[b * ORACLE_Q8_BLOCK_ELEMS + 16 + j]",
+                       "w[b * ORACLE_Q8_BLOCK_ELEMS + 2 * j] = (double)(lo - 8) * d4;\n"
+                       "            w[b * ORACLE_Q8_BLOCK_ELEMS + 2 * j + 1]"),
+    "q4_block_stride": ("#define ORACLE_Q4_BLOCK_BYTES 18", "#define ORACLE_Q4_BLOCK_BYTES 17"),
     "router_index": ("const float* wr = Wr + (size_t)e * dm;", "const float* wr = Wr + (size_t)(E - 1 - e) * dm;"),
 }
 
