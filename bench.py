@@ -36,12 +36,23 @@ sys.path.insert(0, ROOT)
 
 from routed_mixture_experts_router_gb300 import binding, synth  # noqa: E402
 
-Q8_ROW_BYTES = lambda K: (K // 32) * 34  # noqa: E731  bytes of one Q8_0 row in HBM (int8 + fp16 per 32)
+def row_bytes(wl, K: int) -> int:
+    """HBM bytes of one weight row of K values: per 32, 32 int8 (Q8_0) or 16
+    bytes of nibbles (Q4_0), plus one fp16 scale."""
+    return (K // 32) * (18 if wl.wfmt == "q4" else 34)
 
 
 def expert_bytes(wl) -> int:
-    """HBM bytes of one expert's three Q8_0 matrices (qs + scales)."""
-    return 2 * wl.d_ff * Q8_ROW_BYTES(wl.d_model) + wl.d_model * Q8_ROW_BYTES(wl.d_ff)
+    """HBM bytes of one expert's three quantised matrices (values + scales)."""
+    return 2 * wl.d_ff * row_bytes(wl, wl.d_model) + wl.d_model * row_bytes(wl, wl.d_ff)
+
+
+def wfmt_of(wl) -> int:
+    return binding.MOE_WFMT_Q4_0 if wl.wfmt == "q4" else binding.MOE_WFMT_Q8_0
+
+
+def fmt_name(wl) -> str:
+    return "Q4_0" if wl.wfmt == "q4" else "Q8_0"
 
 
 # ------------------------------------------------------------------ dist ----
@@ -162,7 +173,8 @@ def oracle_tokens_per_s(wl, layer_host, x_all: np.ndarray, budget_s: float = 12.
         xb = x_all[rows]
         t0 = time.perf_counter()
         orc.moe_layer(xb, layer_host["Wr"], layer_host["bias"], layer_host["gate"], layer_host["up"],
-                      layer_host["down"], wl.d_model, wl.d_ff, wl.E, wl.k, residual=wl.residual)
+                      layer_host["down"], wl.d_model, wl.d_ff, wl.E, wl.k, residual=wl.residual,
+                      fmt=wfmt_of(wl))
         t_used += time.perf_counter() - t0
         done += batch
         i += batch
@@ -187,7 +199,7 @@ def run_reference(args, ws, rank):
     def step(i):
         xb = xs[i * per_step:(i + 1) * per_step]
         orc.moe_layer(xb, host["Wr"], host["bias"], host["gate"], host["up"], host["down"], wl.d_model, wl.d_ff,
-                      wl.E, wl.k, residual=wl.residual)
+                      wl.E, wl.k, residual=wl.residual, fmt=wfmt_of(wl))
 
     for i in range(args.warmup):
         step(i)
@@ -259,7 +271,7 @@ def graph_kernel_nodes(g):
 
 def workload_config(wl, args):
     return {"workload": f"{wl.name}: one MoE layer, T={wl.T}, d_model={wl.d_model}, d_ff={wl.d_ff}, E={wl.E}, "
-                        f"top-{wl.k}, Q8_0 SwiGLU experts, {wl.act} activations",
+                        f"top-{wl.k}, {fmt_name(wl)} SwiGLU experts, {wl.act} activations",
             "tokens_per_step": wl.T, "layers_rotated": args.rot,
             "l2": f"inputs larger than L2: steps rotate over {args.rot} seeded layers "
                   f"({args.rot} x {wl.E} experts x {expert_bytes(wl)} B resident)",
@@ -282,7 +294,7 @@ def run_ours(args, ws, rank, local):
         if r == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
             host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
         layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
-                                                w["Wr"], w["bias"]))
+                                                w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
         del w
         xs.append(synth.make_x(wl, dev, step=r))
         outs.append(torch.empty(wl.T, wl.d_model, dtype=torch.float32, device=dev))
@@ -419,7 +431,7 @@ def run_ours(args, ws, rank, local):
     achieved = ffn_alg / (ffn_ms_mean / 1e3) / 1e9
     flops = 2.0 * wl.T * wl.k * 3 * wl.d_model * wl.d_ff            # expert contractions per FFN call
     roofline = {"kernel": ("moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)" if tc_path
-                           else "moe_expert_ffn_q8 (gate/up + down, Q8_0 fused, combine fused)"),
+                           else f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": ffn_alg, "launch_ms": ffn_ms_mean,
@@ -508,7 +520,7 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
-            "data": "synthetic (seeded, qwen3_moe geometry, random-init Q8_0)",
+            "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
             "config": workload_config(wl, args),
             "layer_hbm_gbs": layer_gbs, "near_ties": None,
             "separate_path_ms": {"route_and_bucket": rb_ms, "expert_ffn": ffn_ms_mean},
@@ -536,7 +548,7 @@ def run_stack(args, ws, rank, local):
         if l == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
             host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
         layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
-                                                w["Wr"], w["bias"]))
+                                                w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
         del w
     x0 = synth.make_x(wl, dev, step=0)
     bufs = [torch.empty_like(x0), torch.empty_like(x0)]
@@ -626,7 +638,7 @@ def run_stack(args, ws, rank, local):
     alg = float(np.mean(ffn_alg))
     achieved = alg / (ffn_ms_mean / 1e3) / 1e9
     roofline = {"kernel": ("moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)" if tc_path
-                           else "moe_expert_ffn_q8 (gate/up + down, Q8_0 fused, combine fused)"),
+                           else f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": alg, "launch_ms": ffn_ms_mean, "traffic": None,
@@ -667,12 +679,12 @@ def run_stack(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
-            "data": "synthetic (seeded, qwen3_moe geometry, random-init Q8_0)",
+            "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
             "config": {"workload": f"{wl.name}: {L}-layer MoE stack with residual, T={wl.T}, d_model={wl.d_model}, "
                                    f"d_ff={wl.d_ff}, E={wl.E}, top-{wl.k}, Zipf router bias, "
                                    f"{'bf16' if tc_path else 'f32'} expert inputs",
                        "tokens_per_step": wl.T, "layers": L,
-                       "l2": f"inputs larger than L2: {L} resident layers x 128 experts x 5013504 B",
+                       "l2": f"inputs larger than L2: {L} resident layers x {wl.E} experts x {expert_bytes(wl)} B",
                        "parallelism": f"replicas x{ws}", "graph": f"one CUDA graph per step ({L} layers)"},
             "stack_hbm_gbs": step_bytes / (ms_local / args.steps / 1e3) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu_base,

@@ -1,6 +1,6 @@
 /*
  * moe.h -- C ABI of libmoe_gb300.so: a routed Mixture-of-Experts layer with
- * Q8_0 SwiGLU experts, hand-written for NVIDIA GB300 (sm_103a).
+ * Q8_0 (or Q4_0) SwiGLU experts, hand-written for NVIDIA GB300 (sm_103a).
  *
  * The layer (qwen3_moe geometry: d_model 2048, d_ff 768, 128 experts, top-8,
  * 48 layers -- amalgafy.com/evidence, "Historical baseline environment"):
@@ -39,10 +39,21 @@
  *  - Alignment: every float / int32 array 16-byte aligned; qs and d arrays
  *    16-byte aligned; d_model and d_ff multiples of 32.
  *
- * Device weight layout (produced by moe_pack_q8 from the 34-byte blocks):
+ * Device weight layout, Q8_0 (moe_layer_w.wfmt = MOE_WFMT_Q8_0, produced by
+ * moe_pack_q8 from the 34-byte blocks):
  *   qs  int8     [E][rows][K]       the 32 int8 values of each block, along K
  *   d   fp16 bits[E][rows][K/32]    one scale per 32-wide block
+ * Q4_0 (MOE_WFMT_Q4_0, produced by moe_pack_q4 from 18-byte blocks):
+ *   qs  bytes    [E][rows][K/2]     each block's 16 bytes, unchanged: byte j
+ *                                   of block b holds element 32b+j in its low
+ *                                   nibble and 32b+16+j in its high nibble,
+ *                                   unsigned; the weight is (n - 8) * d
+ *   d   fp16 bits[E][rows][K/32]    one scale per 32-wide block
  *   gate, up: rows = d_ff, K = d_model;  down: rows = d_model, K = d_ff.
+ * The pages name a 4-bit expert format as the next execution stage ("Q4
+ * expert execution", amalgafy.com/technical-overview, "Execution
+ * architecture") without giving its layout; Q4_0 here is the plain 4-bit
+ * sibling of Q8_0 (same 32-wide blocks and fp16 scale, values offset by 8).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -78,6 +89,11 @@ extern "C" {
                           of fewer than 128 pairs, or dimensions not multiples of 128, run the
                           fp32 path (more accurate, and memory-bound at that size anyway) */
 
+/* ---- expert weight formats (moe_layer_w.wfmt) ------------------------- */
+#define MOE_WFMT_Q8_0 0 /* every path */
+#define MOE_WFMT_Q4_0 1 /* fp32 lane-per-row kernels, any T; needs d_model % 512 == 0 and d_ff a
+                           multiple of 256 (else MOE_ERR_UNSUPPORTED); MOE_ACT_BF16 runs them too */
+
 /* ---- flags ----------------------------------------------------------- */
 #define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */
 
@@ -86,19 +102,21 @@ extern "C" {
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 32
 
-/* One Q8_0 matrix family (all E experts), device layout above. */
+/* One quantised matrix family (all E experts), device layout above; qs
+ * holds int8 values (Q8_0) or packed nibbles (Q4_0). */
 typedef struct {
     const int8_t* qs;
     const uint16_t* d;
 } moe_q8_mat;
 
 /* One layer's weights.  router_w: fp32 [E][d_model]; router_bias: fp32 [E]
- * or NULL. */
+ * or NULL; wfmt: MOE_WFMT_* of gate, up and down. */
 typedef struct {
     int E, k, d_model, d_ff;
     moe_q8_mat gate, up, down;
     const float* router_w;
     const float* router_bias;
+    int wfmt;
 } moe_layer_w;
 
 /*
@@ -117,6 +135,15 @@ MOE_API size_t moe_workspace_size(int T, const moe_layer_w* w, int act, int flag
  * rows may span several experts ([E*rows_per_expert]).  Bit-exact copy.
  */
 MOE_API int moe_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, void* stream);
+
+/*
+ * Repack Q4_0 weights from 18-byte blocks (fp16 scale d, little endian, then
+ * 16 bytes of 4-bit values, layout above) into the device layout.
+ *   blocks: device bytes, rows * (K/32) blocks, row-major (any alignment)
+ *   qs: bytes [rows][K/2] (16-byte aligned); d: fp16 bits [rows][K/32]
+ * Bit-exact copy.
+ */
+MOE_API int moe_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t* qs, uint16_t* d, void* stream);
 
 /*
  * Router: logits x . Wr^T (+ bias) in fp32, top-k (ties to the lower id,
@@ -142,8 +169,8 @@ MOE_API int moe_bucket(const int32_t* idx, int T, int k, int E, int32_t* offsets
                int32_t* pos, int32_t* status, void* stream);
 
 /*
- * Expert SwiGLU FFNs over the bucketed pairs, Q8_0 dequantisation fused into
- * the contractions.
+ * Expert SwiGLU FFNs over the bucketed pairs, dequantisation (Q8_0 or Q4_0,
+ * w->wfmt) fused into the contractions.
  *   x: fp32 [T][d_model] expert inputs (token-indexed)
  *   offsets, pair_tok, pair_slot, pos, wts: from moe_bucket / moe_route.
  *       Every bucket is clamped into [0, T*k] and token / slot ids are

@@ -25,10 +25,12 @@ MOE_STATUS_TIMEOUT = 2
 MOE_ACT_F32 = 0
 MOE_ACT_BF16 = 1
 MOE_FLAG_DETERMINISTIC = 1
+MOE_WFMT_Q8_0 = 0
+MOE_WFMT_Q4_0 = 1
 
 _ERR = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE"}
 
-ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
+ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_pack_q4", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
                 "moe_layer_forward", "moe_layer_forward_static", "moe_version")
 MOE_STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -46,7 +48,7 @@ class Q8Mat(ctypes.Structure):
 class LayerW(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("k", ctypes.c_int), ("d_model", ctypes.c_int), ("d_ff", ctypes.c_int),
                 ("gate", Q8Mat), ("up", Q8Mat), ("down", Q8Mat), ("router_w", ctypes.c_void_p),
-                ("router_bias", ctypes.c_void_p)]
+                ("router_bias", ctypes.c_void_p), ("wfmt", ctypes.c_int)]
 
 
 _lib = None
@@ -72,6 +74,8 @@ def load(path: str | None = None):
     L.moe_workspace_size.argtypes = [I, LWP, I, I]
     L.moe_pack_q8.restype = I
     L.moe_pack_q8.argtypes = [P, LL, I, P, P, P]
+    L.moe_pack_q4.restype = I
+    L.moe_pack_q4.argtypes = [P, LL, I, P, P, P]
     L.moe_route.restype = I
     L.moe_route.argtypes = [P, I, LWP, P, P, P]
     L.moe_bucket.restype = I
@@ -106,26 +110,33 @@ def _check(fn: str, rc: int):
 class Layer:
     """Device-resident weights of one MoE layer in the library's layout.
 
-    Holds the packed Q8_0 tensors (qs int8 [E][rows][K], d fp16-bits
-    [E][rows][K/32]) and the fp32 router, plus the C struct pointing at them.
+    Holds the packed expert tensors (Q8_0: qs int8 [E][rows][K]; Q4_0: qs
+    uint8 [E][rows][K/2]; d fp16-bits [E][rows][K/32]) and the fp32 router,
+    plus the C struct pointing at them.  wfmt: MOE_WFMT_Q8_0 or MOE_WFMT_Q4_0.
     """
 
-    def __init__(self, E, k, d_model, d_ff, gate, up, down, router_w, router_bias=None):
-        self.E, self.k, self.d_model, self.d_ff = E, k, d_model, d_ff
+    def __init__(self, E, k, d_model, d_ff, gate, up, down, router_w, router_bias=None, wfmt=None):
+        wfmt = MOE_WFMT_Q8_0 if wfmt is None else wfmt
+        self.E, self.k, self.d_model, self.d_ff, self.wfmt = E, k, d_model, d_ff, wfmt
         self.gate, self.up, self.down = gate, up, down          # (qs, d) tuples
         self.router_w = router_w.contiguous()
         self.router_bias = None if router_bias is None else router_bias.contiguous()
         self.c = LayerW(E, k, d_model, d_ff, Q8Mat(gate[0].data_ptr(), gate[1].data_ptr()),
                         Q8Mat(up[0].data_ptr(), up[1].data_ptr()), Q8Mat(down[0].data_ptr(), down[1].data_ptr()),
-                        self.router_w.data_ptr(), 0 if self.router_bias is None else self.router_bias.data_ptr())
+                        self.router_w.data_ptr(), 0 if self.router_bias is None else self.router_bias.data_ptr(),
+                        wfmt)
 
     @classmethod
-    def from_blocks(cls, E, k, d_model, d_ff, gate_blocks, up_blocks, down_blocks, router_w, router_bias=None):
-        """Pack the pages' 34-byte Q8_0 blocks (device uint8 tensors) with moe_pack_q8."""
-        gate = pack_q8(gate_blocks, E * d_ff, d_model)
-        up = pack_q8(up_blocks, E * d_ff, d_model)
-        down = pack_q8(down_blocks, E * d_model, d_ff)
-        return cls(E, k, d_model, d_ff, gate, up, down, router_w, router_bias)
+    def from_blocks(cls, E, k, d_model, d_ff, gate_blocks, up_blocks, down_blocks, router_w, router_bias=None,
+                    wfmt=None):
+        """Pack 34-byte Q8_0 blocks (moe_pack_q8) or, for wfmt MOE_WFMT_Q4_0,
+        18-byte Q4_0 blocks (moe_pack_q4); device uint8 tensors."""
+        wfmt = MOE_WFMT_Q8_0 if wfmt is None else wfmt
+        pack = pack_q4 if wfmt == MOE_WFMT_Q4_0 else pack_q8
+        gate = pack(gate_blocks, E * d_ff, d_model)
+        up = pack(up_blocks, E * d_ff, d_model)
+        down = pack(down_blocks, E * d_model, d_ff)
+        return cls(E, k, d_model, d_ff, gate, up, down, router_w, router_bias, wfmt)
 
     def ref(self):
         return ctypes.byref(self.c)
@@ -141,6 +152,15 @@ def pack_q8(blocks: torch.Tensor, rows: int, K: int):
     qs = torch.empty(rows, K, dtype=torch.int8, device=blocks.device)
     d = torch.empty(rows, K // 32, dtype=torch.int16, device=blocks.device)
     _check("moe_pack_q8", L.moe_pack_q8(_ptr(blocks), rows, K, _ptr(qs), _ptr(d), _stream()))
+    return qs, d
+
+
+def pack_q4(blocks: torch.Tensor, rows: int, K: int):
+    """moe_pack_q4: 18-byte blocks -> (qs uint8 [rows][K/2], d int16-bits [rows][K/32])."""
+    L = load()
+    qs = torch.empty(rows, K // 2, dtype=torch.uint8, device=blocks.device)
+    d = torch.empty(rows, K // 32, dtype=torch.int16, device=blocks.device)
+    _check("moe_pack_q4", L.moe_pack_q4(_ptr(blocks), rows, K, _ptr(qs), _ptr(d), _stream()))
     return qs, d
 
 

@@ -49,7 +49,12 @@ bool valid_geometry(const moe_layer_w* w) {
     if (w->k < 1 || w->k > MOE_MAX_TOPK || w->k > w->E) return false;
     if (w->d_model < 32 || w->d_model % 32 || w->d_model > 8192) return false;
     if (w->d_ff < 32 || w->d_ff % 32 || w->d_ff > 8192) return false;
-    return true;
+    return w->wfmt == MOE_WFMT_Q8_0 || w->wfmt == MOE_WFMT_Q4_0;
+}
+
+// Q4_0 experts run only on the lane-per-row kernels.
+bool wfmt_supported(const moe_layer_w* w) {
+    return w->wfmt == MOE_WFMT_Q8_0 || ffn_rows_supported(*w, 1);
 }
 
 bool valid_T(int T, const moe_layer_w* w) { return T >= 0 && T <= 65536 && (long long)T * w->k <= INT_MAX / 2; }
@@ -90,11 +95,16 @@ int check_device() {
 // least one 128-pair MMA tile (smaller batches run the fp32 path, which is
 // more accurate and memory-bound anyway); fp32 -> for 3+ tokens the
 // lane-per-row kernels, for 1-2 tokens the streaming kernels, where the
-// geometry allows; the per-expert-CTA kernels otherwise.
+// geometry allows; the per-expert-CTA kernels otherwise.  Q4_0 weights: the
+// lane-per-row kernels for every T (the callers have checked the geometry).
 cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, const int32_t* offsets,
                        const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse, float* out,
                        int residual, char* ws, const WsLayout& L, int32_t* status, cudaStream_t s) {
     float* h = reinterpret_cast<float*>(ws + L.h);
+    if (w.wfmt != MOE_WFMT_Q8_0) {
+        if (!ffn_rows_supported(w, T)) return cudaErrorNotSupported;
+        return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
+    }
     if (act == MOE_ACT_BF16 && ffn_tc_supported(w, T))
         return launch_ffn_tc(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual,
                              reinterpret_cast<__nv_bfloat16*>(ws + L.xb), reinterpret_cast<__nv_bfloat16*>(h),
@@ -133,6 +143,15 @@ int moe_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16
     return cuda_rc(launch_pack_q8(blocks, rows, K, qs, d, (cudaStream_t)stream));
 }
 
+int moe_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t* qs, uint16_t* d, void* stream) {
+    if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!blocks || !qs || !d || !aligned16(qs)) return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_pack_q4(blocks, rows, K, qs, d, (cudaStream_t)stream));
+}
+
 int moe_route(const float* x, int T, const moe_layer_w* w, int32_t* idx, float* wts, void* stream) {
     if (!valid_geometry(w) || !valid_T(T, w)) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
@@ -162,6 +181,7 @@ int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t
         !aligned16(out_or_ypairs) || !valid_experts(w))
         return MOE_ERR_INVALID_ARG;
     if (fuse_combine && (const void*)out_or_ypairs == (const void*)x) return MOE_ERR_INVALID_ARG;
+    if (!wfmt_supported(w)) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, *w, act, 0);
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();
@@ -191,6 +211,7 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     if (!x || !out || !aligned16(x) || !aligned16(out) || (const void*)x == (const void*)out || !valid_router(w) ||
         !valid_experts(w))
         return MOE_ERR_INVALID_ARG;
+    if (!wfmt_supported(w)) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, *w, act, flags);
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();

@@ -110,6 +110,7 @@ cudaError_t launch_decode_fused(const float* x, int T, const moe_layer_w& w, int
                                 unsigned int* sync, int32_t* status, cudaStream_t s);
 
 cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
+cudaError_t launch_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t* qs, uint16_t* d, cudaStream_t s);
 
 cudaError_t launch_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int dm,
                            const float* residual, float* out, cudaStream_t s);

@@ -1,8 +1,11 @@
-// Q8_0 expert FFN for batches of 3 or more tokens, one lane per weight row.
+// Quantised expert FFN for batches of 3 or more tokens (Q8_0), or any
+// batch (Q4_0), one lane per weight row.
 //
 // Gate/up "Q8_0-quantised SwiGLU experts" and down + weighted combine
 // (amalgafy.com/technical-overview, "Warm target path"; the gate/up and down
-// geometry of expxa.com/research/reuse-ordering-qualification, "Shape").
+// geometry of expxa.com/research/reuse-ordering-qualification, "Shape"); the
+// 4-bit weights of the next stage, "Q4 expert execution" (same page,
+// "Execution architecture"), as Q4_0 blocks.
 //
 // With several tokens per expert the per-token work is no longer negligible
 // next to the weight stream, and a warp-per-row layout (lanes split K) pays
@@ -32,34 +35,62 @@ namespace {
 using namespace stream;
 
 constexpr int kRowsFT = 32;   // rows per CTA item: one per lane
-constexpr int kRowsKS = 64;   // K per warp stage: two Q8_0 blocks, 4 bytes of scales per row
+constexpr int kRowsKS = 64;   // K per warp stage: two 32-wide blocks, 4 bytes of scales per row
 constexpr int kRowsG = 8;     // pairs per bucket chunk
 constexpr int kRowsNSTG = 4;  // ring stages per warp
-constexpr int kTileBytes = kRowsFT * kRowsKS;       // one matrix's [32 rows][64 B] of a stage
-constexpr int kScaleBytes = kRowsFT * 4;            // its scales: 2 fp16 per row
+constexpr int kScaleBytes = kRowsFT * 4;            // a stage's scales of one matrix: 2 fp16 per row
 constexpr int kGuNW = 8;                            // gate/up warps (K = d_model split 8 ways)
-constexpr int kGuStage = 2 * kTileBytes + 2 * kScaleBytes;
-constexpr int kDnStage = kTileBytes + kScaleBytes;
+
+// Format-dependent stage geometry.  FMT 0 (Q8_0): a row's 64 K of a stage
+// are 64 bytes (four 16-byte chunks of 16 values); FMT 1 (Q4_0): 32 bytes
+// (two 16-byte chunks, each one whole block of 32 nibbles).
+template <int FMT>
+struct RowsFmt {
+    static constexpr int kRowBytes = FMT ? kRowsKS / 2 : kRowsKS;      // bytes of one row per stage
+    static constexpr int kChunks = kRowBytes / 16;                     // 16-byte chunks per row
+    static constexpr int kTileBytes = kRowsFT * kRowBytes;             // one matrix's [32 rows] of a stage
+    static constexpr int kGuStage = 2 * kTileBytes + 2 * kScaleBytes;
+    static constexpr int kDnStage = kTileBytes + kScaleBytes;
+    // Byte offset of 16-byte chunk c of row r in a tile.  Q8_0: rotated by
+    // r/2 over 4 chunks; Q4_0: by r/4 over 2 chunks.  Either way the 8 lanes
+    // of one 16-byte shared-memory phase read 8 different bank groups.
+    static __device__ __forceinline__ int tile_off(int r, int c) {
+        return FMT ? r * kRowBytes + (((c + (r >> 2)) & 1) << 4) : r * kRowBytes + (((c + (r >> 1)) & 3) << 4);
+    }
+};
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Byte offset of 16-byte chunk c (0..3) of row r in a [32][64 B] tile.  The
-// chunk is rotated by r/2, so the 32 lanes' reads of one chunk column touch
-// every 16-byte bank group exactly four times (no bank conflicts).
-__device__ __forceinline__ int tile_off(int r, int c) { return r * kRowsKS + (((c + (r >> 1)) & 3) << 4); }
-
-// Rows row0 .. row0+31, K bytes [k0, k0+64) of one Q8_0 matrix (qs row
-// stride K, scale row stride K/32 halves) into a tile and its scales.
+// Rows row0 .. row0+31, K range [k0, k0+64) of one matrix (qs row stride
+// K bytes for Q8_0, K/2 for Q4_0; scale row stride K/32 halves) into a tile
+// and its scales.
+template <int FMT>
 __device__ __forceinline__ void issue_tile(unsigned char* tile, unsigned char* sc, const int8_t* qs, const uint16_t* d,
                                            size_t row0, int K, int k0, int lane) {
+    using F = RowsFmt<FMT>;
+    const int rb = FMT ? K / 2 : K;  // bytes per weight row
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int pc = lane + 32 * m, r = pc >> 2, c = pc & 3;
-        cp_async16(tile + tile_off(r, c), qs + (row0 + r) * K + k0 + c * 16);
+    for (int m = 0; m < F::kChunks; ++m) {
+        const int pc = lane + 32 * m, r = pc / F::kChunks, c = pc % F::kChunks;
+        cp_async16(tile + F::tile_off(r, c),
+                   reinterpret_cast<const unsigned char*>(qs) + (row0 + r) * rb + (FMT ? k0 / 2 : k0) + c * 16);
     }
     cp_async4(sc + lane * 4, d + (row0 + lane) * (K / 32) + k0 / 32);
+}
+
+// 16 consecutive weights (values 16u .. 16u+15 of a stage row, u = 0..3) of
+// this lane's row, dequantised exactly into 8 fp32 pairs.  Q8_0: chunk u.
+// Q4_0: chunk u/2 holds one block; its low nibbles are the block's values
+// 0..15, its high nibbles 16..31.
+template <int FMT>
+__device__ __forceinline__ void stage_w16(const unsigned char* tile, int lane, int u, float d, f32x2 (&w)[8]) {
+    using F = RowsFmt<FMT>;
+    if (FMT == 0)
+        dequant16(*reinterpret_cast<const uint4*>(tile + F::tile_off(lane, u)), d, w);
+    else
+        dequant16_q4(*reinterpret_cast<const uint4*>(tile + F::tile_off(lane, u >> 1)), u & 1, d, w);
 }
 
 // The fp16 scale of 16-byte chunk c (0..3) from a row's 4-byte scale word.
@@ -77,16 +108,17 @@ __device__ __forceinline__ ulonglong2 ld_pairs(const float* v) { return *reinter
 // token's accumulators are registers and nothing is padded.  Each (row,
 // token) sum is split in two accumulators (even and odd 4-wide steps), which
 // gives at least 4 independent FMA chains even for a single token.
-template <int NT>
+template <int NT, int FMT>
 __device__ __forceinline__ void gu_stage(const unsigned char* st, int lane, const float* xk, const int* xoff,
                                          f32x2 (&ag)[2][kRowsG], f32x2 (&au)[2][kRowsG]) {
-    const uint32_t sgw = reinterpret_cast<const uint32_t*>(st + 2 * kTileBytes)[lane];
-    const uint32_t suw = reinterpret_cast<const uint32_t*>(st + 2 * kTileBytes + kScaleBytes)[lane];
+    constexpr int TB = RowsFmt<FMT>::kTileBytes;
+    const uint32_t sgw = reinterpret_cast<const uint32_t*>(st + 2 * TB)[lane];
+    const uint32_t suw = reinterpret_cast<const uint32_t*>(st + 2 * TB + kScaleBytes)[lane];
 #pragma unroll
     for (int c = 0; c < kRowsKS / 16; ++c) {
         f32x2 wg[8], wu[8];
-        dequant16(*reinterpret_cast<const uint4*>(st + tile_off(lane, c)), chunk_scale(sgw, c), wg);
-        dequant16(*reinterpret_cast<const uint4*>(st + kTileBytes + tile_off(lane, c)), chunk_scale(suw, c), wu);
+        stage_w16<FMT>(st, lane, c, chunk_scale(sgw, c), wg);
+        stage_w16<FMT>(st + TB, lane, c, chunk_scale(suw, c), wu);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -98,14 +130,14 @@ __device__ __forceinline__ void gu_stage(const unsigned char* st, int lane, cons
     }
 }
 
-template <int NT>
+template <int NT, int FMT>
 __device__ __forceinline__ void dn_stage(const unsigned char* st, int lane, const float* hk, int f,
                                          f32x2 (&acc)[2][kRowsG]) {
-    const uint32_t sw = reinterpret_cast<const uint32_t*>(st + kTileBytes)[lane];
+    const uint32_t sw = reinterpret_cast<const uint32_t*>(st + RowsFmt<FMT>::kTileBytes)[lane];
 #pragma unroll
     for (int c = 0; c < kRowsKS / 16; ++c) {
         f32x2 wv[8];
-        dequant16(*reinterpret_cast<const uint4*>(st + tile_off(lane, c)), chunk_scale(sw, c), wv);
+        stage_w16<FMT>(st, lane, c, chunk_scale(sw, c), wv);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -133,7 +165,7 @@ __device__ __forceinline__ void dn_stage(const unsigned char* st, int lane, cons
 // w owns K range [w*dm/8, (w+1)*dm/8), SPI = dm/512 stages per item.
 // ALLTOK: every token's x staged once (T <= 8); else the chunk's x is staged
 // per chunk (restaged at chunk changes).
-template <bool ALLTOK>
+template <bool ALLTOK, int FMT>
 __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
     const uint16_t* __restrict__ gd, const int8_t* __restrict__ uqs, const uint16_t* __restrict__ ud,
@@ -148,6 +180,7 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
     const int d4 = dm / 4;
     const int kw = dm / kGuNW, spi = kw / kRowsKS;
     const int ftn = f / kRowsFT;
+    constexpr int kGuStage = RowsFmt<FMT>::kGuStage, TB = RowsFmt<FMT>::kTileBytes;
     unsigned char* ring = gr_smem + (size_t)warp * kRowsNSTG * kGuStage;
     float* xs = reinterpret_cast<float*>(gr_smem + (size_t)kGuNW * kRowsNSTG * kGuStage);  // [8 or T][dm]
     float* part = xs + (size_t)kRowsG * dm;  // [8 warps][8 pairs][gate, up][32]
@@ -190,8 +223,8 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
             }
             const int k0 = warp * kw + is_s * kRowsKS;
             unsigned char* st = ring + (size_t)slot * kGuStage;
-            issue_tile(st, st + 2 * kTileBytes, gqs, gd, is_row0, dm, k0, lane);
-            issue_tile(st + kTileBytes, st + 2 * kTileBytes + kScaleBytes, uqs, ud, is_row0, dm, k0, lane);
+            issue_tile<FMT>(st, st + 2 * TB, gqs, gd, is_row0, dm, k0, lane);
+            issue_tile<FMT>(st + TB, st + 2 * TB + kScaleBytes, uqs, ud, is_row0, dm, k0, lane);
             if (++is_s == spi) {
                 is_s = 0;
                 ++is_i;
@@ -241,7 +274,7 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
         {
             const unsigned char* st = ring + (size_t)(q % kRowsNSTG) * kGuStage;
             const float* xk = xs + warp * kw + s * kRowsKS;
-#define MOE_GU_STAGE(NT) gu_stage<NT>(st, lane, xk, xoff, ag, au)
+#define MOE_GU_STAGE(NT) gu_stage<NT, FMT>(st, lane, xk, xoff, ag, au)
             MOE_ROWS_SWITCH(n, MOE_GU_STAGE)
 #undef MOE_GU_STAGE
         }
@@ -281,7 +314,7 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
 // Items: (bucket chunk g, output tile ot) with d_model/32 tiles per chunk.
 // NW warps split K = d_ff (NW * 64 | d_ff), SPI = d_ff / (NW * 64).  The
 // chunk's h rows, tokens and routing weights are staged per chunk.
-template <int NW>
+template <int NW, int FMT>
 __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
     const float* __restrict__ h, int T, int f, int dm, int E, int k, const int8_t* __restrict__ dqs,
     const uint16_t* __restrict__ dd, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok,
@@ -296,6 +329,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
     const int f4 = f / 4;
     const int kw = f / NW, spi = kw / kRowsKS;
     const int otn = dm / kRowsFT;
+    constexpr int kDnStage = RowsFmt<FMT>::kDnStage;
     unsigned char* ring = dr_smem + (size_t)warp * kRowsNSTG * kDnStage;
     float* hs = reinterpret_cast<float*>(dr_smem + (size_t)NW * kRowsNSTG * kDnStage);  // [8][f]
     float* part = hs + (size_t)kRowsG * f;                                             // [NW][8][32]
@@ -320,7 +354,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
                 is_row0 = (size_t)s_act[is_a] * dm + (size_t)(is_i - g * otn) * kRowsFT;
             }
             unsigned char* st = ring + (size_t)slot * kDnStage;
-            issue_tile(st, st + kTileBytes, dqs, dd, is_row0, f, warp * kw + is_s * kRowsKS, lane);
+            issue_tile<FMT>(st, st + RowsFmt<FMT>::kTileBytes, dqs, dd, is_row0, f, warp * kw + is_s * kRowsKS, lane);
             if (++is_s == spi) {
                 is_s = 0;
                 ++is_i;
@@ -366,7 +400,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
         {
             const unsigned char* st = ring + (size_t)(q % kRowsNSTG) * kDnStage;
             const float* hk = hs + warp * kw + s * kRowsKS;
-#define MOE_DN_STAGE(NT) dn_stage<NT>(st, lane, hk, f, acc)
+#define MOE_DN_STAGE(NT) dn_stage<NT, FMT>(st, lane, hk, f, acc)
             MOE_ROWS_SWITCH(n, MOE_DN_STAGE)
 #undef MOE_DN_STAGE
         }
@@ -436,23 +470,29 @@ int down_rows_warps(int f) {
     return 0;
 }
 
-size_t gateup_rows_smem(int dm) {
-    return (size_t)kGuNW * kRowsNSTG * kGuStage + (size_t)kRowsG * dm * 4 + (size_t)kGuNW * kRowsG * 2 * 32 * 4;
+size_t gateup_rows_smem(int dm, int fmt) {
+    const size_t stage = fmt ? RowsFmt<1>::kGuStage : RowsFmt<0>::kGuStage;
+    return (size_t)kGuNW * kRowsNSTG * stage + (size_t)kRowsG * dm * 4 + (size_t)kGuNW * kRowsG * 2 * 32 * 4;
 }
 
-size_t down_rows_smem(int f, int nw) {
-    return (size_t)nw * kRowsNSTG * kDnStage + (size_t)kRowsG * f * 4 + (size_t)nw * kRowsG * 32 * 4;
+size_t down_rows_smem(int f, int nw, int fmt) {
+    const size_t stage = fmt ? RowsFmt<1>::kDnStage : RowsFmt<0>::kDnStage;
+    return (size_t)nw * kRowsNSTG * stage + (size_t)kRowsG * f * 4 + (size_t)nw * kRowsG * 32 * 4;
 }
 
 constexpr size_t kRowsSmemCap = 220 * 1024;
 
 }  // namespace
 
+// Q8_0 from 3 tokens on (1-2 tokens stream faster with a warp per row);
+// Q4_0 for every T, these being its only kernels.
 bool ffn_rows_supported(const moe_layer_w& w, int T) {
-    if (T < 3) return false;
+    if (w.wfmt != MOE_WFMT_Q8_0 && w.wfmt != MOE_WFMT_Q4_0) return false;
+    if (T < 3 && w.wfmt == MOE_WFMT_Q8_0) return false;
     if (w.d_model % (kGuNW * kRowsKS) != 0 || w.d_ff % kRowsFT != 0 || w.d_model % kRowsFT != 0) return false;
     const int nw = down_rows_warps(w.d_ff);
-    return nw != 0 && gateup_rows_smem(w.d_model) <= kRowsSmemCap && down_rows_smem(w.d_ff, nw) <= kRowsSmemCap;
+    return nw != 0 && gateup_rows_smem(w.d_model, w.wfmt) <= kRowsSmemCap &&
+           down_rows_smem(w.d_ff, nw, w.wfmt) <= kRowsSmemCap;
 }
 
 cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
@@ -462,21 +502,28 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
     const int P = T * w.k;
     float* out_init = fuse_combine ? out_or_ypairs : nullptr;
     const bool alltok = T <= kRowsG && P <= kMaxStagedPairs;
-    const size_t gsm = gateup_rows_smem(w.d_model);
-    cudaError_t err =
-        alltok ? launch_rows(gateup_rows_kernel<true>, kGuNW * 32, gsm, s, x, T, w.d_model, w.d_ff, w.E, w.gate.qs,
-                             w.gate.d, w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P)
-               : launch_rows(gateup_rows_kernel<false>, kGuNW * 32, gsm, s, x, T, w.d_model, w.d_ff, w.E, w.gate.qs,
-                             w.gate.d, w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P);
+    const int fmt = w.wfmt;
+    const size_t gsm = gateup_rows_smem(w.d_model, fmt);
+#define MOE_GU_ROWS(AT, FM)                                                                                       \
+    launch_rows(gateup_rows_kernel<AT, FM>, kGuNW * 32, gsm, s, x, T, w.d_model, w.d_ff, w.E, w.gate.qs, w.gate.d, \
+                w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P)
+    cudaError_t err = fmt ? (alltok ? MOE_GU_ROWS(true, 1) : MOE_GU_ROWS(false, 1))
+                          : (alltok ? MOE_GU_ROWS(true, 0) : MOE_GU_ROWS(false, 0));
+#undef MOE_GU_ROWS
     if (err != cudaSuccess) return err;
     const int nw = down_rows_warps(w.d_ff);
-    const size_t dsm = down_rows_smem(w.d_ff, nw);
-#define MOE_DOWN_ROWS(NW)                                                                                    \
-    launch_rows(down_rows_kernel<NW>, NW * 32, dsm, s, h, T, w.d_ff, w.d_model, w.E, w.k, w.down.qs, w.down.d, \
+    const size_t dsm = down_rows_smem(w.d_ff, nw, fmt);
+#define MOE_DOWN_ROWS(NW, FM)                                                                                      \
+    launch_rows(down_rows_kernel<NW, FM>, NW * 32, dsm, s, h, T, w.d_ff, w.d_model, w.E, w.k, w.down.qs, w.down.d, \
                 offsets, pair_tok, pair_slot, wts, fuse_combine, out_or_ypairs)
-    if (nw == 12) return MOE_DOWN_ROWS(12);
-    if (nw == 8) return MOE_DOWN_ROWS(8);
-    return MOE_DOWN_ROWS(4);
+    if (fmt) {
+        if (nw == 12) return MOE_DOWN_ROWS(12, 1);
+        if (nw == 8) return MOE_DOWN_ROWS(8, 1);
+        return MOE_DOWN_ROWS(4, 1);
+    }
+    if (nw == 12) return MOE_DOWN_ROWS(12, 0);
+    if (nw == 8) return MOE_DOWN_ROWS(8, 0);
+    return MOE_DOWN_ROWS(4, 0);
 #undef MOE_DOWN_ROWS
 #undef MOE_ROWS_SWITCH
 }

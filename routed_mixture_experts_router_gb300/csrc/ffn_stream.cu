@@ -341,7 +341,7 @@ cudaError_t down_dispatch(const float* h, int T, const moe_layer_w& w, const int
 bool ffn_stream_supported(const moe_layer_w& w) {
     // whole 16-byte pieces of weights and of each row's scales: K % 256 == 0;
     // down items are 4 whole rows; at most 4 chunks per lane.
-    return w.d_model % 256 == 0 && w.d_ff % 256 == 0 && w.d_model % kDnRowsPerItem == 0 && w.d_model <= 2048 &&
+    return w.wfmt == MOE_WFMT_Q8_0 && w.d_model % 256 == 0 && w.d_ff % 256 == 0 && w.d_model % kDnRowsPerItem == 0 && w.d_model <= 2048 &&
            w.d_ff <= 1024;
 }
 

@@ -563,7 +563,7 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
 }  // namespace
 
 bool ffn_tc_supported(const moe_layer_w& w, int T) {
-    return w.d_model % kBKR == 0 && w.d_ff % kBKR == 0 && w.d_model % kBM == 0 && w.d_ff % kBM == 0 &&
+    return w.wfmt == MOE_WFMT_Q8_0 && w.d_model % kBKR == 0 && w.d_ff % kBKR == 0 && w.d_model % kBM == 0 && w.d_ff % kBM == 0 &&
            (long long)T * w.k >= kBN && encode_fn() != nullptr;
 }
 

@@ -24,6 +24,22 @@ __global__ void pack_q8_kernel(const uint8_t* __restrict__ blocks, long long nbl
     dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
 }
 
+// One 18-byte Q4_0 block per thread: the scale to d, the 16 nibble bytes
+// unchanged to qs (the device layout keeps the block's own nibble order).
+__global__ void pack_q4_kernel(const uint8_t* __restrict__ blocks, long long nblocks, uint8_t* __restrict__ qs,
+                               uint16_t* __restrict__ d) {
+    const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t* src = blocks + b * 18;
+    d[b] = (uint16_t)(src[0] | (src[1] << 8));
+    uint32_t wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        wv[i] = (uint32_t)src[2 + 4 * i] | ((uint32_t)src[3 + 4 * i] << 8) | ((uint32_t)src[4 + 4 * i] << 16) |
+                ((uint32_t)src[5 + 4 * i] << 24);
+    reinterpret_cast<uint4*>(qs)[b] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
 // out[t][o] = (residual ? residual[t][o] : 0) + sum_{s<k} wts[t][s] * ypairs[pos[t][s]][o], s ascending.
 // ("weighted combine", amalgafy.com/technical-overview, "Execution architecture")
 __global__ void combine_kernel(const float* __restrict__ ypairs, const float* __restrict__ wts,
@@ -54,6 +70,15 @@ cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t*
     const int threads = 256;
     const long long grid = (nb + threads - 1) / threads;
     pack_q8_kernel<<<(unsigned)grid, threads, 0, s>>>(blocks, nb, qs, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t* qs, uint16_t* d, cudaStream_t s) {
+    const long long nb = rows * (K / 32);
+    if (nb == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long grid = (nb + threads - 1) / threads;
+    pack_q4_kernel<<<(unsigned)grid, threads, 0, s>>>(blocks, nb, qs, d);
     return cudaGetLastError();
 }
 

@@ -58,6 +58,28 @@ __device__ __forceinline__ void dequant16(const uint4 q, float d, f32x2 (&w)[8])
     }
 }
 
+// 16 Q4_0 weights times their block scale d, exactly, as 8 fp32 pairs: the
+// low (half 0) or high (half 1) nibbles of a 16-byte block, values n in
+// 0..15.  As above, v = 2^15 + n and fma(v, d, -(2^15 + 8) d) = (n - 8) d:
+// the constant has 13 x 11 significant bits (exact in fp32) and the result
+// at most 15, so the fma's one rounding changes nothing.
+__device__ __forceinline__ void dequant16_q4(const uint4 q, int half, float d, f32x2 (&w)[8]) {
+    const f32x2 dd = f2_pack(d, d);
+    const float c = -32776.0f * d;
+    const f32x2 cc = f2_pack(c, c);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t u = (half ? words[m] >> 4 : words[m]) & 0x0f0f0f0fu;
+        w[2 * m] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
+                                  __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
+                          dd, cc);
+        w[2 * m + 1] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7524)),
+                                      __uint_as_float(__byte_perm(u, 0x47000000u, 0x7534))),
+                              dd, cc);
+    }
+}
+
 // sum over 16 values of (q * d) * x: one 16-byte weight chunk dequantised
 // with its block scale d (exactly), four float4 of x at stride `st`.
 __device__ __forceinline__ float chunk_dot_scaled(const uint4 q, float d, const float4* xv4, int st) {

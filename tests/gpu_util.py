@@ -25,11 +25,15 @@ class Case:
     host: dict            # numpy copies for the oracle
 
 
+def wfmt_of(wl: synth.Workload) -> int:
+    return binding.MOE_WFMT_Q4_0 if wl.wfmt == "q4" else binding.MOE_WFMT_Q8_0
+
+
 def make_case(wl: synth.Workload, layer_id: int = 0, step: int = 0, T: int | None = None) -> Case:
     w = synth.make_layer(wl, layer_id, "cuda")
     x = synth.make_x(wl, "cuda", step, T)
     lay = binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"], w["Wr"],
-                                    w["bias"])
+                                    w["bias"], wfmt=wfmt_of(wl))
     torch.cuda.synchronize()
     host = {
         "x": x.double().cpu().numpy(),
@@ -49,7 +53,8 @@ def oracle_layer(case: Case, tokens=None, forced_idx=None, residual=False, bf16=
         xv = xv[tokens]
     wl = case.wl
     return oracle.get().moe_layer(xv, h["Wr"], h["bias"], h["gate"], h["up"], h["down"], wl.d_model, wl.d_ff, wl.E,
-                                  wl.k, residual=residual, expert_input_bf16=bf16, forced_idx=forced_idx)
+                                  wl.k, residual=residual, expert_input_bf16=bf16, forced_idx=forced_idx,
+                                  fmt=wfmt_of(wl))
 
 
 def near_tie_mask(logits: np.ndarray, k: int) -> np.ndarray:

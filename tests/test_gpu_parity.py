@@ -4,6 +4,8 @@ Routing indices and bucket results bit-exact (near-tie tokens counted and
 checked as valid selections), layer outputs within max relative L2 1e-5 on
 the fp32-activation path.
 """
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -32,7 +34,8 @@ SHAPES = [
 
 
 def _wl(name, T, d, f, E, k, zipf):
-    return synth.custom(name, wid=hash(name) % 10000 + 200, T=T, d_model=d, d_ff=f, E=E, k=k, zipf=zipf)
+    return synth.custom(name, wid=zlib.crc32(name.encode()) % 10000 + 200,
+                        T=T, d_model=d, d_ff=f, E=E, k=k, zipf=zipf)
 
 
 @pytest.fixture(scope="module", autouse=True)
