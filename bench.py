@@ -439,7 +439,7 @@ def run_ours(args, ws, rank, local):
     if fused_step:
         step_alg0 = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
         fa = step_alg0 / (fused_ms / 1e3) / 1e9
-        roofline = {"kernel": "decode_fused_kernel (whole layer: router, top-k, bucketing, Q8_0 gate/up + down, "
+        roofline = {"kernel": f"decode_fused_kernel (whole layer: router, top-k, bucketing, {fmt_name(wl)} gate/up + down, "
                               "combine; one cooperative launch)",
                     "bound": "hbm", "achieved": fa, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": fa / peaks["hbm_gbs"], "peak_source": peaks["source"],

@@ -1,7 +1,7 @@
 // The whole MoE layer for one or two decode tokens in ONE cooperative launch:
-// router GEMV -> top-k -> bucketing -> Q8_0 gate/up + SwiGLU -> Q8_0 down +
-// weighted combine ("router -> resident expert -> combine -> next layer",
-// amalgafy.com/technical-overview, "Warm target path").
+// router GEMV -> top-k -> bucketing -> gate/up + SwiGLU -> down + weighted
+// combine, Q8_0 or Q4_0 experts ("router -> resident expert -> combine ->
+// next layer", amalgafy.com/technical-overview, "Warm target path").
 //
 // At T = 1 a layer moves ~41 MB and the separate kernels spend much of their
 // time in launch ramps, prologues that must first learn the routed experts,
@@ -79,7 +79,18 @@ __device__ void grid_barrier(unsigned int* count, unsigned int target, int32_t* 
     __syncthreads();
 }
 
-template <int KG, int KD, int G>
+// Per-format geometry.  Q8_0: 16-value chunks, 4-row down items (16 lanes per
+// row); Q4_0: 32-value blocks, 8-row down items (8 lanes per row).
+template <int FMT>
+struct FuFmt {
+    static constexpr int kCF4 = FMT ? 8 : 4;         // float4 of activations per 16-byte weight chunk
+    static constexpr int kDnRows = FMT ? kDnRowsPerItemQ4 : kDnRowsPerItem;
+    static constexpr int kDnLPR = FMT ? 8 : 16;      // lanes per down row
+    static __host__ __device__ int gu_bytes(int dm) { return (FMT ? dm : 2 * dm) + 2 * (dm / 16); }
+    static __host__ __device__ int dn_bytes(int f) { return kDnRows * (FMT ? f / 2 : f) + kDnRows * (f / 16); }
+};
+
+template <int KG, int KD, int G, int FMT>
 __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams p) {
     extern __shared__ __align__(128) unsigned char fsm[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
@@ -90,13 +101,15 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
     __shared__ float s_pw[kFuMaxP];
     __shared__ __align__(16) float s_lg[kFuMaxT][MOE_MAX_EXPERTS];
 
-    constexpr int kXTok4 = KG * 4 * 32;  // float4 per staged token (gate/up layout)
-    constexpr int kHTok4 = KD * 4 * 16;  // float4 per staged pair (down layout)
+    using F = FuFmt<FMT>;
+    constexpr int CF4 = F::kCF4;
+    constexpr int kXTok4 = KG * CF4 * 32;        // float4 per staged token (gate/up layout)
+    constexpr int kHTok4 = KD * CF4 * F::kDnLPR;  // float4 per staged pair (down layout)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = p.T, dm = p.dm, f = p.f, E = p.E, k = p.k;
     const int P = T * k, d4 = dm / 4, f4 = f / 4;
-    const int gu_bytes = 2 * dm + 2 * (dm / 16);
-    const int dn_bytes = kDnRowsPerItem * f + kDnRowsPerItem * (f / 16);
+    const int gu_bytes = F::gu_bytes(dm);
+    const int dn_bytes = F::dn_bytes(f);
     const int item_bytes = gu_bytes > dn_bytes ? gu_bytes : dn_bytes;
     unsigned char* ring = fsm + (size_t)warp * kFuNSTG * item_bytes;
     float4* act = reinterpret_cast<float4*>(fsm + (size_t)kFuNW * kFuNSTG * item_bytes);  // x, later h
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
     pdl_wait();
     for (int i = threadIdx.x; i < T * d4; i += kFuThreads) {
         const int t = i / d4, q = i - t * d4;
-        act[t * kXTok4 + stage_idx<32>(q)] = __ldcg(reinterpret_cast<const float4*>(p.x) + (size_t)t * d4 + q);
+        act[t * kXTok4 + stage_idx<32, CF4>(q)] = __ldcg(reinterpret_cast<const float4*>(p.x) + (size_t)t * d4 + q);
     }
     for (int i = blockIdx.x * kFuThreads + threadIdx.x; i < T * d4; i += gridDim.x * kFuThreads)
         reinterpret_cast<float4*>(p.out)[i] =
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
 #pragma unroll
                 for (int t = 0; t < kFuMaxT; ++t)
                     if (t < T) {
-                        const float4 xv = act[t * kXTok4 + stage_idx<32>(q)];
+                        const float4 xv = act[t * kXTok4 + stage_idx<32, CF4>(q)];
                         acc[t] = fmaf(wv[u].x, xv.x,
                                       fmaf(wv[u].y, xv.y, fmaf(wv[u].z, xv.z, fmaf(wv[u].w, xv.w, acc[t]))));
                     }
@@ -210,26 +223,36 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
         item_range(s_cb[s_n] * f, &lo, &hi);
         auto issue = [&](int i, int st) {
             const int g = i / f, r = i - g * f;
-            gu_issue_item<KG>(ring + (size_t)st * item_bytes, p.gqs, p.uqs, p.gd, p.ud,
-                              (size_t)s_act[locate(g, s_cb, s_n)] * f + r, dm, lane);
+            const size_t row = (size_t)s_act[locate(g, s_cb, s_n)] * f + r;
+            if constexpr (FMT == 1)
+                gu_issue_item_q4<KG>(ring + (size_t)st * item_bytes, p.gqs, p.uqs, p.gd, p.ud, row, dm, lane);
+            else
+                gu_issue_item<KG>(ring + (size_t)st * item_bytes, p.gqs, p.uqs, p.gd, p.ud, row, dm, lane);
         };
         auto compute = [&](int i, int st) {
             const int g = i / f, r = i - g * f;
             const int a = locate(g, s_cb, s_n);
-            gu_compute_item<KG, G, true>(ring + (size_t)st * item_bytes, r, s_beg[a], s_end[a], dm, f, lane, act,
-                                         s_ptok, p.h);
+            if constexpr (FMT == 1)
+                gu_compute_item_q4<KG, G>(ring + (size_t)st * item_bytes, r, s_beg[a], s_end[a], dm, f, lane, act,
+                                          s_ptok, p.h);
+            else
+                gu_compute_item<KG, G, true>(ring + (size_t)st * item_bytes, r, s_beg[a], s_end[a], dm, f, lane,
+                                             act, s_ptok, p.h);
         };
         warp_stream<kFuNSTG>(lo + warp, hi, kFuNW, issue, compute);
     }
 
     // 5. down items: put the first ones in flight, wait for every CTA's h, stage h
-    const int nq = dm / kDnRowsPerItem;
+    const int nq = dm / F::kDnRows;
     int lo, hi;
     item_range(s_cb[s_n] * nq, &lo, &hi);
     auto dissue = [&](int i, int st) {
         const int g = i / nq, qd = i - g * nq;
-        dn_issue_item(ring + (size_t)st * item_bytes, p.dqs, p.dd,
-                      (size_t)s_act[locate(g, s_cb, s_n)] * dm + (size_t)qd * kDnRowsPerItem, f, lane);
+        const size_t row0 = (size_t)s_act[locate(g, s_cb, s_n)] * dm + (size_t)qd * F::kDnRows;
+        if constexpr (FMT == 1)
+            dn_issue_item_q4(ring + (size_t)st * item_bytes, p.dqs, p.dd, row0, f, lane);
+        else
+            dn_issue_item(ring + (size_t)st * item_bytes, p.dqs, p.dd, row0, f, lane);
     };
     const int first = lo + warp;
     const int n = first < hi ? (hi - first + kFuNW - 1) / kFuNW : 0;
@@ -241,10 +264,11 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
     grid_barrier(p.sync, 2, p.status);
     for (int q = threadIdx.x; q < P * f4; q += kFuThreads) {
         const int pp = q / f4, qq = q - pp * f4;
-        act[pp * kHTok4 + stage_idx<16>(qq)] = __ldcg(reinterpret_cast<const float4*>(p.h) + (size_t)pp * f4 + qq);
+        act[pp * kHTok4 + stage_idx<F::kDnLPR, CF4>(qq)] =
+            __ldcg(reinterpret_cast<const float4*>(p.h) + (size_t)pp * f4 + qq);
     }
     __syncthreads();
-    const int hl = lane & 15, sub = lane >> 4;
+    const int hl = lane & (F::kDnLPR - 1), sub = lane / F::kDnLPR;
     for (int j = 0; j < n; ++j) {
         const int jn = j + kFuNSTG - 1;
         if (jn < n) dissue(first + jn * kFuNW, jn % kFuNSTG);
@@ -254,8 +278,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
         const int i = first + j * kFuNW;
         const int g = i / nq, qd = i - g * nq;
         const int a = locate(g, s_cb, s_n);
-        dn_compute_item<KD, G, true>(ring + (size_t)(j % kFuNSTG) * item_bytes, qd, s_beg[a], s_end[a], f, dm, k, T,
-                                     hl, sub, act, s_ptok, s_pw, nullptr, nullptr, nullptr, 1, p.out);
+        if constexpr (FMT == 1)
+            dn_compute_item_q4<KD, G>(ring + (size_t)(j % kFuNSTG) * item_bytes, qd, s_beg[a], s_end[a], f, dm, hl,
+                                      sub, act, s_ptok, s_pw, p.out);
+        else
+            dn_compute_item<KD, G, true>(ring + (size_t)(j % kFuNSTG) * item_bytes, qd, s_beg[a], s_end[a], f, dm,
+                                         k, T, hl, sub, act, s_ptok, s_pw, nullptr, nullptr, nullptr, 1, p.out);
         __syncwarp();
     }
     cp_async_wait<0>();
@@ -268,15 +296,15 @@ int fused_num_sms() {
     return n > 0 ? n : 148;
 }
 
-template <int KG, int KD, int G>
+template <int KG, int KD, int G, int FMT>
 cudaError_t launch_fused(const FusedParams& p, cudaStream_t s) {
-    const int gu = 2 * p.dm + 2 * (p.dm / 16);
-    const int dn = kDnRowsPerItem * p.f + kDnRowsPerItem * (p.f / 16);
+    using F = FuFmt<FMT>;
+    const int gu = F::gu_bytes(p.dm), dn = F::dn_bytes(p.f);
     const size_t ring = (size_t)kFuNW * kFuNSTG * (gu > dn ? gu : dn);
-    const size_t xs = (size_t)p.T * KG * 4 * 32 * 16, hs = (size_t)p.T * p.k * KD * 4 * 16 * 16;
+    const size_t xs = (size_t)p.T * KG * F::kCF4 * 32 * 16, hs = (size_t)p.T * p.k * KD * F::kCF4 * F::kDnLPR * 16;
     const size_t smem = ring + (xs > hs ? xs : hs);
     if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
-    auto kern = decode_fused_kernel<KG, KD, G>;
+    auto kern = decode_fused_kernel<KG, KD, G, FMT>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
@@ -300,9 +328,13 @@ cudaError_t launch_fused(const FusedParams& p, cudaStream_t s) {
 }  // namespace
 
 bool decode_fused_supported(const moe_layer_w& w, int T) {
-    // the routing phase holds all T*k pairs in one warp's lanes
-    return T >= 1 && T <= kFuMaxT && T * w.k <= 32 && ffn_stream_supported(w) && w.d_model <= 2048 &&
-           w.d_ff <= 1024;
+    // the routing phase holds all T*k pairs in one warp's lanes; items are
+    // whole 16-byte pieces of weights and scales (K % 256 == 0) and whole
+    // down items; at most 4 weight chunks per lane
+    if (w.wfmt != MOE_WFMT_Q8_0 && w.wfmt != MOE_WFMT_Q4_0) return false;
+    const int rows = w.wfmt == MOE_WFMT_Q4_0 ? kDnRowsPerItemQ4 : kDnRowsPerItem;
+    return T >= 1 && T <= kFuMaxT && T * w.k <= 32 && w.d_model % 256 == 0 && w.d_ff % 256 == 0 &&
+           w.d_model % rows == 0 && w.d_model <= 2048 && w.d_ff <= 1024;
 }
 
 cudaError_t launch_decode_fused(const float* x, int T, const moe_layer_w& w, int residual, float* out,
@@ -332,10 +364,23 @@ cudaError_t launch_decode_fused(const float* x, int T, const moe_layer_w& w, int
     p.wts_out = wts_out;
     p.offsets_out = offsets_out;
     p.status = status;
+    if (w.wfmt == MOE_WFMT_Q4_0) {
+        // blocks per lane: gate/up d_model/1024, down d_ff/256 (rounded up)
+        const int kg = (w.d_model / 32 + 31) / 32, kd = (w.d_ff / 32 + 7) / 8;
+#define MOE_FUSED_GO4(KG, KD) \
+    return T == 1 ? launch_fused<KG, KD, 1, 1>(p, s) : launch_fused<KG, KD, 2, 1>(p, s)
+        if (kg == 2 && kd == 3) MOE_FUSED_GO4(2, 3);
+        if (kg == 2 && kd == 4) MOE_FUSED_GO4(2, 4);
+        if (kg == 2 && kd == 2) MOE_FUSED_GO4(2, 2);
+        if (kg == 1 && kd == 2) MOE_FUSED_GO4(1, 2);
+        if (kg == 1 && kd == 1) MOE_FUSED_GO4(1, 1);
+#undef MOE_FUSED_GO4
+        return cudaErrorInvalidConfiguration;
+    }
     // chunks per lane: gate/up d_model/512, down d_ff/256 (rounded up)
     const int kg = (w.d_model / 16 + 31) / 32, kd = (w.d_ff / 16 + 15) / 16;
 #define MOE_FUSED_GO(KG, KD) \
-    return T == 1 ? launch_fused<KG, KD, 1>(p, s) : launch_fused<KG, KD, 2>(p, s)
+    return T == 1 ? launch_fused<KG, KD, 1, 0>(p, s) : launch_fused<KG, KD, 2, 0>(p, s)
     if (kg == 4 && kd == 3) MOE_FUSED_GO(4, 3);
     if (kg == 4 && kd == 4) MOE_FUSED_GO(4, 4);
     if (kg == 4 && kd == 2) MOE_FUSED_GO(4, 2);

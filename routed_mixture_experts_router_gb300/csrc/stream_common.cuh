@@ -105,12 +105,13 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Shared-memory layout of one staged activation vector for LPR lanes that
-// split K in 16-value chunks c = hl + LPR*m: float4 j of chunk c sits at
-// (m*4 + j)*LPR + hl, so one load instruction reads consecutive float4s.
-template <int LPR>
+// split K in chunks of CF4 float4 (16 values for Q8_0 chunks, 32 for Q4_0
+// blocks), chunk c = hl + LPR*m: float4 j of chunk c sits at
+// (m*CF4 + j)*LPR + hl, so one load instruction reads consecutive float4s.
+template <int LPR, int CF4 = 4>
 __device__ __forceinline__ int stage_idx(int q) {
-    const int c = q >> 2, j = q & 3;
-    return ((c / LPR) * 4 + j) * LPR + (c % LPR);
+    const int c = q / CF4, j = q % CF4;
+    return ((c / LPR) * CF4 + j) * LPR + (c % LPR);
 }
 
 // Active experts (non-empty buckets) in id order, by warp 0, and the work
@@ -351,6 +352,169 @@ __device__ __forceinline__ void dn_compute_item(const unsigned char* b, int qd, 
                 } else {
                     out[(size_t)p * dm + o] = y;
                 }
+            }
+        }
+    }
+}
+
+// ---- Q4_0 work items (the fused decode kernel) -------------------------------
+// A 16-byte chunk is one whole Q4_0 block (32 values, one scale).  Down items
+// are 8 rows, two per quarter-warp, so that a row's d_ff/32 blocks spread over
+// 8 lanes as evenly as a Q8_0 row's d_ff/16 chunks over 16.
+constexpr int kDnRowsPerItemQ4 = 8;
+
+// sum over the 32 values of one Q4_0 block of w * x: low nibbles against
+// float4 0..3 of the chunk, high nibbles against float4 4..7 (stride st).
+__device__ __forceinline__ float chunk_dot_q4(const uint4 q, float d, const float4* xv4, int st) {
+    f32x2 w[8];
+    f32x2 acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        dequant16_q4(q, half, d, w);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float4 xv = xv4[(4 * half + m) * st];
+            acc0 = f2_fma(w[2 * m], f2_pack(xv.x, xv.y), acc0);
+            acc1 = f2_fma(w[2 * m + 1], f2_pack(xv.z, xv.w), acc1);
+        }
+    }
+    return f2_sum(f2_add(acc0, acc1));
+}
+
+// gate/up item of feature `row`: its Q4_0 gate row and up row (dm/2 bytes
+// each), then their fp16 scales (dm/32 each).
+template <int KCH>
+__device__ __forceinline__ void gu_issue_item_q4(unsigned char* b, const int8_t* gqs, const int8_t* uqs,
+                                                 const uint16_t* gd, const uint16_t* ud, size_t row, int dm,
+                                                 int lane) {
+    const int nch = dm / 32, rb = dm / 2;
+    const unsigned char* g = reinterpret_cast<const unsigned char*>(gqs) + row * rb;
+    const unsigned char* u = reinterpret_cast<const unsigned char*>(uqs) + row * rb;
+#pragma unroll
+    for (int m = 0; m < KCH; ++m) {
+        const int c = lane + 32 * m;
+        if (c < nch) {
+            cp_async16(b + c * 16, g + c * 16);
+            cp_async16(b + rb + c * 16, u + c * 16);
+        }
+    }
+    const int sp = dm / 256;  // 16-byte pieces of one row's scales
+    const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(gd) + row * (dm / 16);
+    const unsigned char* usrc = reinterpret_cast<const unsigned char*>(ud) + row * (dm / 16);
+    if (lane < sp) cp_async16(b + dm + lane * 16, gsrc + lane * 16);
+    else if (lane < 2 * sp) cp_async16(b + dm + dm / 16 + (lane - sp) * 16, usrc + (lane - sp) * 16);
+    cp_async_commit();
+}
+
+// h[p][r] = silu(g) * u for the pairs p in [pb, pe) of feature r; xs holds
+// every token's activations in the 32-value chunk layout (stage_idx<32, 8>).
+template <int KCH, int G>
+__device__ __forceinline__ void gu_compute_item_q4(const unsigned char* b, int r, int pb, int pe, int dm, int f,
+                                                   int lane, const float4* xs, const int* s_tok, float* h) {
+    constexpr int kTok4 = KCH * 8 * 32;
+    const int nch = dm / 32, rb = dm / 2;
+    const __half* gsc = reinterpret_cast<const __half*>(b + dm);
+    const __half* usc = gsc + dm / 32;
+    for (int pp = pb; pp < pe; pp += G) {
+        const int ng = min(G, pe - pp);
+        int toff[G];
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) toff[g2] = (g2 < ng ? s_tok[pp + g2] : 0) * kTok4;
+        float ga[G], ua[G];
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) {
+            ga[g2] = 0.f;
+            ua[g2] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < KCH; ++m) {
+            const int c = lane + 32 * m;
+            if (c < nch) {
+                const uint4 qg = *reinterpret_cast<const uint4*>(b + c * 16);
+                const uint4 qu = *reinterpret_cast<const uint4*>(b + rb + c * 16);
+                const float sg = __half2float(gsc[c]), su = __half2float(usc[c]);
+#pragma unroll
+                for (int g2 = 0; g2 < G; ++g2) {
+                    if (g2 < ng) {
+                        const float4* xv = xs + toff[g2] + m * 8 * 32 + lane;
+                        ga[g2] += chunk_dot_q4(qg, sg, xv, 32);
+                        ua[g2] += chunk_dot_q4(qu, su, xv, 32);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) {
+            ga[g2] = warp_sum(ga[g2]);
+            ua[g2] = warp_sum(ua[g2]);
+        }
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2)
+            if (lane == g2 && g2 < ng) h[(size_t)(pp + g2) * f + r] = silu_f(ga[g2]) * ua[g2];
+    }
+}
+
+// down item: Q4_0 rows row0 .. row0+7 of Wd (contiguous, f/2 bytes each),
+// then their scales (f/32 each).
+__device__ __forceinline__ void dn_issue_item_q4(unsigned char* b, const int8_t* dqs, const uint16_t* dd,
+                                                 size_t row0, int f, int lane) {
+    const int qbytes = kDnRowsPerItemQ4 * f / 2;
+    const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(dqs) + row0 * (f / 2);
+    for (int pc = lane; pc < qbytes / 16; pc += 32) cp_async16(b + pc * 16, qsrc + pc * 16);
+    const int spieces = kDnRowsPerItemQ4 * f / 256;  // 8 rows x f/32 fp16 scales, in 16-byte pieces
+    const unsigned char* ssrc = reinterpret_cast<const unsigned char*>(dd) + row0 * (f / 16);
+    if (lane < spieces) cp_async16(b + qbytes + lane * 16, ssrc + lane * 16);
+    cp_async_commit();
+}
+
+// y = Wd[o] . h[p] for the 8 rows o = 8*qd.. of a landed Q4_0 down item and
+// the pairs p in [pb, pe), combined into out with the staged pair tokens and
+// weights.  Quarter warp `sub` owns rows 2*sub, 2*sub+1; hs: every pair's h
+// in the 32-value chunk layout for 8 lanes (stage_idx<8, 8>).
+template <int KCH, int G>
+__device__ __forceinline__ void dn_compute_item_q4(const unsigned char* b, int qd, int pb, int pe, int f, int dm,
+                                                   int hl, int sub, const float4* hs, const int* s_ptok,
+                                                   const float* s_pw, float* out) {
+    constexpr int LPR = 8;
+    constexpr int kTok4 = KCH * 8 * LPR;
+    const int nch = f / 32, rb = f / 2;
+    const __half* sc = reinterpret_cast<const __half*>(b + kDnRowsPerItemQ4 * rb);
+    for (int pp = pb; pp < pe; pp += G) {
+        const int ng = min(G, pe - pp);
+        int hoff[G];
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) hoff[g2] = (g2 < ng ? pp + g2 : 0) * kTok4;
+        float acc[2][G];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int g2 = 0; g2 < G; ++g2) acc[rr][g2] = 0.f;
+#pragma unroll
+        for (int m = 0; m < KCH; ++m) {
+            const int c = hl + LPR * m;
+            if (c < nch) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int rl = sub * 2 + rr;
+                    const uint4 q = *reinterpret_cast<const uint4*>(b + (size_t)rl * rb + c * 16);
+                    const float s = __half2float(sc[rl * nch + c]);
+#pragma unroll
+                    for (int g2 = 0; g2 < G; ++g2)
+                        if (g2 < ng) acc[rr][g2] += chunk_dot_q4(q, s, hs + hoff[g2] + m * 8 * LPR + hl, LPR);
+                }
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int g2 = 0; g2 < G; ++g2) acc[rr][g2] = group_sum<LPR>(acc[rr][g2]);
+#pragma unroll
+        for (int g2 = 0; g2 < G; ++g2) {
+            if (g2 < ng && hl < 2) {
+                const int o = qd * kDnRowsPerItemQ4 + sub * 2 + hl;  // lane 0 / 1 of the quarter: row 0 / 1
+                const float y = hl == 0 ? acc[0][g2] : acc[1][g2];
+                const int tok = s_ptok[pp + g2];
+                if (tok >= 0) atomicAdd(out + (size_t)tok * dm + o, s_pw[pp + g2] * y);
             }
         }
     }
