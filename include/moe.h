@@ -82,6 +82,8 @@ extern "C" {
 #define MOE_STATUS_BAD_INDEX 1 /* an expert id outside [0, E), or repeated in one token */
 #define MOE_STATUS_TIMEOUT 2   /* a bounded on-device wait (grid barrier, mbarrier) gave up after
                                   2 s; that call's outputs are invalid */
+#define MOE_STATUS_ARENA_FULL 4 /* an arena admission had more missed experts than evictable slots;
+                                   the experts left without a slot are skipped (wrong outputs) */
 
 /* ---- expert-input precision ------------------------------------------ */
 #define MOE_ACT_F32 0  /* fp32 activations, CUDA-core Q8_0 contraction (decode) */
@@ -110,13 +112,20 @@ typedef struct {
 } moe_q8_mat;
 
 /* One layer's weights.  router_w: fp32 [E][d_model]; router_bias: fp32 [E]
- * or NULL; wfmt: MOE_WFMT_* of gate, up and down. */
+ * or NULL; wfmt: MOE_WFMT_* of gate, up and down.
+ * expert_slot (device int32 [E]) or NULL: with NULL, gate/up/down hold the E
+ * experts in expert order; otherwise they are an expert arena of n_slots
+ * slots ([n_slots][rows][...]) and expert e's matrices sit in slot
+ * expert_slot[e] (moe_arena_admit writes such a map).  A slot outside
+ * [0, n_slots) means "not resident": that expert's pairs are skipped. */
 typedef struct {
     int E, k, d_model, d_ff;
     moe_q8_mat gate, up, down;
     const float* router_w;
     const float* router_bias;
     int wfmt;
+    int n_slots;
+    const int32_t* expert_slot;
 } moe_layer_w;
 
 /*
@@ -248,6 +257,91 @@ MOE_API int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int a
 #define MOE_STATIC_SCRATCH_BYTES (8u << 20)
 MOE_API int moe_layer_forward_static(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual,
                                      float* out, int32_t* status, void* stream);
+
+/*
+ * ---- Expert arena: device-resident slots with a host-memory miss path ----
+ *
+ * "Managed VRAM expert arena" and the miss path that "changes residency
+ * beneath the compute plane" (amalgafy.com/technical-overview, "VRAM budget
+ * policy", "Execution architecture"), reduced to one GPU: every expert of
+ * every layer lives in host memory as one page-aligned blob; the arena holds
+ * n_slots of them in HBM.  Each layer call admits the experts its bucketing
+ * routes to: hits keep their slot, misses take the least recently used
+ * evictable slots and their blobs are copied in by the GPU itself, reading
+ * the page-locked host memory directly (on GB300 host memory is coherent
+ * with the GPU over NVLink-C2C), so no host synchronisation or readback is
+ * involved and the admission can be captured in a CUDA graph.
+ *
+ * Replacement (one admission, for layer l with active experts A ascending):
+ *   clock += 1; every resident e in A: its slot's stamp = clock (a hit);
+ *   the missed experts, ascending, take the evictable slots (stamp != clock)
+ *   in ascending (stamp, slot) order -- empty slots have stamp 0 -- evicting
+ *   their previous owners; each taken slot's stamp = clock.
+ *
+ * Blob (host memory, moe_arena_blob_bytes() each, blob index l*E + e): a
+ * 4 KiB header page (uint32 words: magic 0x424f454d, version 1, wfmt,
+ * layer, expert, d_model, d_ff, payload bytes) and the payload: gate qs,
+ * up qs, down qs, gate d, up d, down d of that expert, in the device layout
+ * above, back to back, the whole blob a multiple of 4 KiB.  For Q8_0 at
+ * d_model 2048, d_ff 768 the payload is 5,013,504 B and the blob 5,017,600 B.
+ *
+ * State (device memory, moe_arena_state_bytes()): starts with
+ * moe_arena_stats, then the residency tables; the caller may read the
+ * stats whenever it likes (e.g. with a device-to-host copy).
+ */
+typedef struct {
+    unsigned long long hits;      /* admitted experts that were resident */
+    unsigned long long misses;    /* admitted experts copied in */
+    unsigned long long bytes_in;  /* payload bytes copied from host memory */
+    unsigned int clock;           /* admissions so far */
+    int layers, experts, slots;
+    int last_misses;              /* misses of the latest admission */
+    int full_events;              /* admissions that ran out of evictable slots */
+    int reserved[2];
+} moe_arena_stats;
+
+/* Bytes of one expert blob for the geometry and format of w (0 if invalid). */
+MOE_API size_t moe_arena_blob_bytes(const moe_layer_w* w);
+
+/* Device bytes of the arena state for `layers` x `experts` and `slots` (0 if invalid;
+ * experts <= 256, slots <= 65536). */
+MOE_API size_t moe_arena_state_bytes(int layers, int experts, int slots);
+
+/* Reset the state: every slot empty, clock and stats zero. */
+MOE_API int moe_arena_init(void* state, int layers, int experts, int slots, void* stream);
+
+/*
+ * Write the blob of expert e of layer `layer` from a layer's resident weights
+ * w (device layout, expert order; w->expert_slot must be NULL) into `blob`
+ * (device memory, or page-locked host memory the GPU can address).
+ */
+MOE_API int moe_arena_pack_blob(const moe_layer_w* w, int layer, int e, void* blob, void* stream);
+
+/*
+ * One admission (replacement rule above) for layer `layer`, whose bucketing
+ * is `offsets` (int32 [E+1], buckets clamped into [0, P]).
+ *   host_blobs: the blobs of all layers x experts, blob index l*E + e
+ *       (page-locked host memory, or device memory), read by the GPU
+ *   arena: geometry, format and the slot arrays (gate/up/down with
+ *       arena->n_slots slots); its expert_slot is ignored
+ *   slot_map: int32 [E] out, the map for the FFN (arena->expert_slot):
+ *       every admitted expert's slot, -1 for experts left without one
+ *   status: optional; MOE_STATUS_ARENA_FULL when misses exceed the evictable slots
+ * Two kernels: the admission (one CTA) and the copy of the missed blobs.
+ */
+MOE_API int moe_arena_admit(void* state, int layer, const int32_t* offsets, int P, const void* host_blobs,
+                            const moe_layer_w* arena, int32_t* slot_map, int32_t* status, void* stream);
+
+/*
+ * The layer forward through the arena: route -> bucket -> admit -> expert
+ * FFNs reading the arena slots -> combine.  Same arguments as
+ * moe_layer_forward, plus the arena state, the layer index and the host
+ * blobs; w is the arena (router of this layer, gate/up/down with n_slots
+ * slots).  Never takes the single-launch decode kernel.
+ */
+MOE_API int moe_layer_forward_arena(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual,
+                                    float* out, void* state, int layer, const void* host_blobs, void* ws,
+                                    size_t ws_bytes, int32_t* status, void* stream);
 
 /* Library version string (static storage). */
 MOE_API const char* moe_version(void);

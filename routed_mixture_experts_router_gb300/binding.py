@@ -22,6 +22,7 @@ MOE_ERR_CUDA = 3
 MOE_ERR_WORKSPACE = 4
 MOE_STATUS_BAD_INDEX = 1
 MOE_STATUS_TIMEOUT = 2
+MOE_STATUS_ARENA_FULL = 4
 MOE_ACT_F32 = 0
 MOE_ACT_BF16 = 1
 MOE_FLAG_DETERMINISTIC = 1
@@ -30,7 +31,8 @@ MOE_WFMT_Q4_0 = 1
 
 _ERR = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE"}
 
-ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_pack_q4", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
+ENTRY_POINTS = ("moe_workspace_size", "moe_pack_q8", "moe_pack_q4", "moe_arena_blob_bytes", "moe_arena_state_bytes",
+                "moe_arena_init", "moe_arena_pack_blob", "moe_arena_admit", "moe_layer_forward_arena", "moe_route", "moe_bucket", "moe_expert_ffn_q8", "moe_combine",
                 "moe_layer_forward", "moe_layer_forward_static", "moe_version")
 MOE_STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -48,7 +50,14 @@ class Q8Mat(ctypes.Structure):
 class LayerW(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("k", ctypes.c_int), ("d_model", ctypes.c_int), ("d_ff", ctypes.c_int),
                 ("gate", Q8Mat), ("up", Q8Mat), ("down", Q8Mat), ("router_w", ctypes.c_void_p),
-                ("router_bias", ctypes.c_void_p), ("wfmt", ctypes.c_int)]
+                ("router_bias", ctypes.c_void_p), ("wfmt", ctypes.c_int), ("n_slots", ctypes.c_int),
+                ("expert_slot", ctypes.c_void_p)]
+
+
+class ArenaStats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_ulonglong), ("misses", ctypes.c_ulonglong), ("bytes_in", ctypes.c_ulonglong),
+                ("clock", ctypes.c_uint), ("layers", ctypes.c_int), ("experts", ctypes.c_int), ("slots", ctypes.c_int),
+                ("last_misses", ctypes.c_int), ("full_events", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
 
 
 _lib = None
@@ -76,6 +85,18 @@ def load(path: str | None = None):
     L.moe_pack_q8.argtypes = [P, LL, I, P, P, P]
     L.moe_pack_q4.restype = I
     L.moe_pack_q4.argtypes = [P, LL, I, P, P, P]
+    L.moe_arena_blob_bytes.restype = SZ
+    L.moe_arena_blob_bytes.argtypes = [LWP]
+    L.moe_arena_state_bytes.restype = SZ
+    L.moe_arena_state_bytes.argtypes = [I, I, I]
+    L.moe_arena_init.restype = I
+    L.moe_arena_init.argtypes = [P, I, I, I, P]
+    L.moe_arena_pack_blob.restype = I
+    L.moe_arena_pack_blob.argtypes = [LWP, I, I, P, P]
+    L.moe_arena_admit.restype = I
+    L.moe_arena_admit.argtypes = [P, I, P, I, P, LWP, P, P, P]
+    L.moe_layer_forward_arena.restype = I
+    L.moe_layer_forward_arena.argtypes = [P, I, LWP, I, I, I, P, P, I, P, P, SZ, P, P]
     L.moe_route.restype = I
     L.moe_route.argtypes = [P, I, LWP, P, P, P]
     L.moe_bucket.restype = I
@@ -115,16 +136,18 @@ class Layer:
     plus the C struct pointing at them.  wfmt: MOE_WFMT_Q8_0 or MOE_WFMT_Q4_0.
     """
 
-    def __init__(self, E, k, d_model, d_ff, gate, up, down, router_w, router_bias=None, wfmt=None):
+    def __init__(self, E, k, d_model, d_ff, gate, up, down, router_w, router_bias=None, wfmt=None, n_slots=0,
+                 expert_slot=None):
         wfmt = MOE_WFMT_Q8_0 if wfmt is None else wfmt
         self.E, self.k, self.d_model, self.d_ff, self.wfmt = E, k, d_model, d_ff, wfmt
+        self.n_slots, self.expert_slot = n_slots, expert_slot
         self.gate, self.up, self.down = gate, up, down          # (qs, d) tuples
         self.router_w = router_w.contiguous()
         self.router_bias = None if router_bias is None else router_bias.contiguous()
         self.c = LayerW(E, k, d_model, d_ff, Q8Mat(gate[0].data_ptr(), gate[1].data_ptr()),
                         Q8Mat(up[0].data_ptr(), up[1].data_ptr()), Q8Mat(down[0].data_ptr(), down[1].data_ptr()),
                         self.router_w.data_ptr(), 0 if self.router_bias is None else self.router_bias.data_ptr(),
-                        wfmt)
+                        wfmt, n_slots, 0 if expert_slot is None else expert_slot.data_ptr())
 
     @classmethod
     def from_blocks(cls, E, k, d_model, d_ff, gate_blocks, up_blocks, down_blocks, router_w, router_bias=None,
@@ -239,4 +262,99 @@ def layer_forward_static(x, layer: Layer, act=MOE_ACT_F32, flags=0, residual=Fal
         out = torch.empty(T, layer.d_model, dtype=torch.float32, device=x.device)
     _check("moe_layer_forward_static", load().moe_layer_forward_static(
         _ptr(x), T, layer.ref(), act, flags, int(bool(residual)), _ptr(out), _ptr(status), _stream()))
+    return out
+
+
+# ------------------------------------------------------------- expert arena --
+class Arena:
+    """An expert arena: `slots` HBM slots for the experts of `layers` layers of
+    one geometry and format, the residency state (moe_arena_state_bytes) and
+    every expert's blob in page-locked host memory (blob l*E + e).
+
+    template: any Layer of that geometry/format (only its shape is used).
+    """
+
+    def __init__(self, template: Layer, layers: int, slots: int, device="cuda"):
+        L = load()
+        self.E, self.k, self.d_model, self.d_ff, self.wfmt = (template.E, template.k, template.d_model,
+                                                              template.d_ff, template.wfmt)
+        self.layers, self.slots = layers, slots
+        f, dm = self.d_ff, self.d_model
+        q4 = self.wfmt == MOE_WFMT_Q4_0
+        u8 = torch.uint8 if q4 else torch.int8
+
+        def mat(rows, K):
+            return (torch.empty(slots, rows, K // 2 if q4 else K, dtype=u8, device=device),
+                    torch.empty(slots, rows, K // 32, dtype=torch.int16, device=device))
+        self.gate, self.up, self.down = mat(f, dm), mat(f, dm), mat(dm, f)
+        self.blob_bytes = int(L.moe_arena_blob_bytes(template.ref()))
+        if self.blob_bytes == 0:
+            raise MoeError("moe_arena_blob_bytes", MOE_ERR_INVALID_ARG)
+        n = int(L.moe_arena_state_bytes(layers, self.E, slots))
+        if n == 0:
+            raise MoeError("moe_arena_state_bytes", MOE_ERR_INVALID_ARG)
+        self.state = torch.empty(n, dtype=torch.uint8, device=device)
+        self.host_blobs = torch.empty(layers * self.E * self.blob_bytes, dtype=torch.uint8, pin_memory=True)
+        self.reset()
+
+    def reset(self):
+        _check("moe_arena_init", load().moe_arena_init(_ptr(self.state), self.layers, self.E, self.slots, _stream()))
+
+    def blob(self, layer: int, e: int) -> torch.Tensor:
+        i = layer * self.E + e
+        return self.host_blobs[i * self.blob_bytes:(i + 1) * self.blob_bytes]
+
+    def pack_layer(self, layer: int, weights: Layer):
+        """Write every expert blob of layer `layer` from resident weights (expert order)."""
+        L = load()
+        for e in range(self.E):
+            _check("moe_arena_pack_blob", L.moe_arena_pack_blob(weights.ref(), layer, e,
+                                                                ctypes.c_void_p(self.blob(layer, e).data_ptr()),
+                                                                _stream()))
+
+    def layer(self, router_w, router_bias=None, slot_map=None) -> Layer:
+        """A Layer over the arena slots with this router (slot_map: the FFN's expert -> slot map, or None)."""
+        return Layer(self.E, self.k, self.d_model, self.d_ff, self.gate, self.up, self.down, router_w, router_bias,
+                     self.wfmt, n_slots=self.slots, expert_slot=slot_map)
+
+    def stats(self) -> dict:
+        raw = self.state[:ctypes.sizeof(ArenaStats)].cpu().numpy().tobytes()
+        st = ArenaStats.from_buffer_copy(raw)
+        return {k: getattr(st, k) for k, _ in ArenaStats._fields_ if k != "reserved"}
+
+    def tables(self):
+        """(slot_of [L][E], owner [S], stamp [S]) as host arrays (layout of include/moe.h's arena state)."""
+        def a256(v):
+            return (v + 255) & ~255
+        o = a256(ctypes.sizeof(ArenaStats))
+        n_so = self.layers * self.E
+        slot_of = self.state[o:o + 4 * n_so].view(torch.int32).cpu().numpy().reshape(self.layers, self.E)
+        o = a256(o + 4 * n_so)
+        owner = self.state[o:o + 4 * self.slots].view(torch.int32).cpu().numpy()
+        o = a256(o + 4 * self.slots)
+        stamp = self.state[o:o + 4 * self.slots].view(torch.int32).cpu().numpy().view("uint32")
+        return slot_of, owner, stamp
+
+
+def arena_admit(arena: Arena, layer: int, offsets: torch.Tensor, P: int, arena_layer: Layer, slot_map=None,
+                status=None):
+    """moe_arena_admit: returns the expert -> slot map (int32 [E])."""
+    if slot_map is None:
+        slot_map = torch.empty(arena.E, dtype=torch.int32, device=offsets.device)
+    _check("moe_arena_admit", load().moe_arena_admit(
+        _ptr(arena.state), layer, _ptr(offsets), P, ctypes.c_void_p(arena.host_blobs.data_ptr()),
+        arena_layer.ref(), _ptr(slot_map), _ptr(status), _stream()))
+    return slot_map
+
+
+def layer_forward_arena(x, arena_layer: Layer, arena: Arena, layer: int, act=MOE_ACT_F32, flags=0, residual=False,
+                        out=None, ws=None, status=None):
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, arena_layer.d_model, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(T, arena_layer, act, flags, x.device)
+    _check("moe_layer_forward_arena", load().moe_layer_forward_arena(
+        _ptr(x), T, arena_layer.ref(), act, flags, int(bool(residual)), _ptr(out), _ptr(arena.state), layer,
+        ctypes.c_void_p(arena.host_blobs.data_ptr()), _ptr(ws), ws.numel(), _ptr(status), _stream()))
     return out

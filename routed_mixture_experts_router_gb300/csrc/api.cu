@@ -16,7 +16,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsLayout {
-    size_t idx, wts, off, ptok, pslot, pos, h, xb, ypairs, lg, sync, total;
+    size_t idx, wts, off, ptok, pslot, pos, h, xb, ypairs, lg, sync, smap, total;
 };
 
 // Workspace carve-up shared by every entry point: the routing results, the
@@ -39,6 +39,7 @@ WsLayout ws_layout(int T, const moe_layer_w& w, int act, int flags) {
     if (flags & MOE_FLAG_DETERMINISTIC) o = align_up(o + P * (size_t)w.d_model * sizeof(float));
     L.lg = o;     o = align_up(o + (size_t)T * w.E * sizeof(float));         // router logits (fused decode)
     L.sync = o;   o = align_up(o + 2 * sizeof(unsigned int));               // grid-barrier words (fused decode)
+    L.smap = o;   o = align_up(o + (size_t)w.E * sizeof(int32_t));           // expert -> arena slot map
     L.total = o;
     return L;
 }
@@ -52,12 +53,18 @@ bool valid_geometry(const moe_layer_w* w) {
     return w->wfmt == MOE_WFMT_Q8_0 || w->wfmt == MOE_WFMT_Q4_0;
 }
 
-// Q4_0 experts run only on the lane-per-row kernels.
-bool wfmt_supported(const moe_layer_w* w) {
-    return w->wfmt == MOE_WFMT_Q8_0 || ffn_rows_supported(*w, 1);
+// Whether launch_ffn has a kernel for this call: Q4_0 experts run only on
+// the lane-per-row kernels; an arena slot map only on the kernels that
+// resolve it (lane-per-row, streaming, tensor-core), not on the fallback.
+bool ffn_supported(const moe_layer_w* w, int T, int act) {
+    if (w->wfmt == MOE_WFMT_Q4_0) return ffn_rows_supported(*w, T > 0 ? T : 1);
+    if (!w->expert_slot) return true;
+    return (act == MOE_ACT_BF16 && ffn_tc_supported(*w, T)) || ffn_rows_supported(*w, T) || ffn_stream_supported(*w);
 }
 
 bool valid_T(int T, const moe_layer_w* w) { return T >= 0 && T <= 65536 && (long long)T * w->k <= INT_MAX / 2; }
+
+bool valid_arena(const moe_layer_w* arena) { return arena->n_slots >= 1 && arena->n_slots <= 65536; }
 
 bool valid_router(const moe_layer_w* w) {
     return w->router_w && aligned16(w->router_w) && (!w->router_bias || aligned16(w->router_bias));
@@ -67,6 +74,7 @@ bool valid_experts(const moe_layer_w* w) {
     const moe_q8_mat* m[3] = {&w->gate, &w->up, &w->down};
     for (auto* q : m)
         if (!q->qs || !q->d || !aligned16(q->qs) || !aligned16(q->d)) return false;
+    if (w->expert_slot && (w->n_slots < 1 || w->n_slots > 65536)) return false;
     return true;
 }
 
@@ -113,6 +121,7 @@ cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, con
         return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
     if (ffn_stream_supported(w))
         return launch_ffn_stream(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, status, s);
+    if (w.expert_slot) return cudaErrorNotSupported;  // the per-expert-CTA kernels read weights in expert order
     return launch_ffn_f32(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
 }
 
@@ -120,6 +129,44 @@ inline int cuda_rc(cudaError_t e) {
     if (e == cudaSuccess) return MOE_OK;
     cudaGetLastError();
     return MOE_ERR_CUDA;
+}
+
+// An arena admission between the bucketing and the expert kernels.
+struct ArenaCall {
+    void* state;
+    int layer;
+    const void* host_blobs;
+};
+
+// Router (+ bucketing), optionally the arena admission, the expert FFNs and
+// the combine.  idx, wts, off: where the routing and bucketing go.
+cudaError_t layer_chain(const float* x, int T, const moe_layer_w& w, int act, int flags, int residual, float* out,
+                        int32_t* idx, float* wts, int32_t* off, char* base, const WsLayout& L, int32_t* status,
+                        const ArenaCall* arena, cudaStream_t s) {
+    int32_t* ptok = reinterpret_cast<int32_t*>(base + L.ptok);
+    int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
+    int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
+    bool bucketed = false;
+    cudaError_t e = launch_route(x, T, w, idx, wts, off, ptok, pslot, pos, &bucketed, s);
+    if (e != cudaSuccess) return e;
+    if (!bucketed) {
+        e = launch_bucket(idx, T, w.k, w.E, off, ptok, pslot, pos, status, s);
+        if (e != cudaSuccess) return e;
+    }
+    moe_layer_w wf = w;
+    if (arena) {
+        int32_t* smap = reinterpret_cast<int32_t*>(base + L.smap);
+        e = launch_arena_admit(arena->state, arena->layer, off, T * w.k, arena->host_blobs, w, smap, status, s);
+        if (e != cudaSuccess) return e;
+        wf.expert_slot = smap;
+    }
+    if (flags & MOE_FLAG_DETERMINISTIC) {
+        float* yp = reinterpret_cast<float*>(base + L.ypairs);
+        e = launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 0, yp, 0, base, L, status, s);
+        if (e != cudaSuccess) return e;
+        return launch_combine(yp, wts, pos, T, w.k, w.d_model, residual ? x : nullptr, out, s);
+    }
+    return launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 1, out, residual, base, L, status, s);
 }
 
 }  // namespace
@@ -181,7 +228,7 @@ int moe_expert_ffn_q8(const float* x, int T, const moe_layer_w* w, const int32_t
         !aligned16(out_or_ypairs) || !valid_experts(w))
         return MOE_ERR_INVALID_ARG;
     if (fuse_combine && (const void*)out_or_ypairs == (const void*)x) return MOE_ERR_INVALID_ARG;
-    if (!wfmt_supported(w)) return MOE_ERR_UNSUPPORTED;
+    if (!ffn_supported(w, T, act)) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, *w, act, 0);
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();
@@ -211,7 +258,7 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     if (!x || !out || !aligned16(x) || !aligned16(out) || (const void*)x == (const void*)out || !valid_router(w) ||
         !valid_experts(w))
         return MOE_ERR_INVALID_ARG;
-    if (!wfmt_supported(w)) return MOE_ERR_UNSUPPORTED;
+    if (!ffn_supported(w, T, act)) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, *w, act, flags);
     if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
     int rc = check_device();
@@ -221,9 +268,6 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + L.idx);
     float* wts = wts_out ? wts_out : reinterpret_cast<float*>(base + L.wts);
     int32_t* off = offsets_out ? offsets_out : reinterpret_cast<int32_t*>(base + L.off);
-    int32_t* ptok = reinterpret_cast<int32_t*>(base + L.ptok);
-    int32_t* pslot = reinterpret_cast<int32_t*>(base + L.pslot);
-    int32_t* pos = reinterpret_cast<int32_t*>(base + L.pos);
     // One or two decode tokens on the fp32 path: the whole layer in one
     // cooperative launch (falls through to the separate kernels if the device
     // cannot co-schedule it).
@@ -237,22 +281,71 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
         if (fe != cudaErrorCooperativeLaunchTooLarge && fe != cudaErrorInvalidConfiguration) return cuda_rc(fe);
         cudaGetLastError();
     }
-    bool bucketed = false;
-    cudaError_t e = launch_route(x, T, *w, idx, wts, off, ptok, pslot, pos, &bucketed, s);
-    if (e != cudaSuccess) return cuda_rc(e);
-    if (!bucketed) {
-        e = launch_bucket(idx, T, w->k, w->E, off, ptok, pslot, pos, status, s);
-        if (e != cudaSuccess) return cuda_rc(e);
+    return cuda_rc(layer_chain(x, T, *w, act, flags, residual, out, idx, wts, off, base, L, status, nullptr, s));
+}
+
+size_t moe_arena_blob_bytes(const moe_layer_w* w) {
+    if (!valid_geometry(w)) return 0;
+    return arena_blob_bytes(*w);
+}
+
+size_t moe_arena_state_bytes(int layers, int experts, int slots) { return arena_state_bytes(layers, experts, slots); }
+
+int moe_arena_init(void* state, int layers, int experts, int slots, void* stream) {
+    if (!state || arena_state_bytes(layers, experts, slots) == 0 || (reinterpret_cast<uintptr_t>(state) & 255u))
+        return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_arena_init(state, layers, experts, slots, (cudaStream_t)stream));
+}
+
+int moe_arena_pack_blob(const moe_layer_w* w, int layer, int e, void* blob, void* stream) {
+    if (!valid_geometry(w) || !valid_experts(w) || w->expert_slot) return MOE_ERR_INVALID_ARG;
+    if (layer < 0 || e < 0 || e >= w->E || !blob || !aligned16(blob)) return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_arena_pack_blob(*w, layer, e, blob, (cudaStream_t)stream));
+}
+
+int moe_arena_admit(void* state, int layer, const int32_t* offsets, int P, const void* host_blobs,
+                    const moe_layer_w* arena, int32_t* slot_map, int32_t* status, void* stream) {
+    if (!valid_geometry(arena) || !valid_arena(arena)) return MOE_ERR_INVALID_ARG;
+    moe_layer_w a = *arena;
+    a.expert_slot = nullptr;
+    if (!valid_experts(&a) || !state || (reinterpret_cast<uintptr_t>(state) & 255u) || !offsets || P < 0 ||
+        !host_blobs || !aligned16(host_blobs) || !slot_map || layer < 0)
+        return MOE_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(launch_arena_admit(state, layer, offsets, P, host_blobs, a, slot_map, status, (cudaStream_t)stream));
+}
+
+int moe_layer_forward_arena(const float* x, int T, const moe_layer_w* w, int act, int flags, int residual,
+                            float* out, void* state, int layer, const void* host_blobs, void* ws, size_t ws_bytes,
+                            int32_t* status, void* stream) {
+    if (!valid_geometry(w) || !valid_T(T, w) || !valid_arena(w)) return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_F32 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    moe_layer_w a = *w;
+    a.expert_slot = nullptr;
+    if (!x || !out || !aligned16(x) || !aligned16(out) || (const void*)x == (const void*)out || !valid_router(w) ||
+        !valid_experts(&a) || !state || (reinterpret_cast<uintptr_t>(state) & 255u) || !host_blobs ||
+        !aligned16(host_blobs) || layer < 0)
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, *w, act, flags);
+    if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_WORKSPACE;
+    {
+        moe_layer_w probe = a;
+        probe.expert_slot = reinterpret_cast<const int32_t*>(static_cast<char*>(ws) + L.smap);
+        if (!ffn_supported(&probe, T, act)) return MOE_ERR_UNSUPPORTED;
     }
-    if (flags & MOE_FLAG_DETERMINISTIC) {
-        float* yp = reinterpret_cast<float*>(base + L.ypairs);
-        e = launch_ffn(x, T, *w, act, off, ptok, pslot, wts, 0, yp, 0, base, L, status, s);
-        if (e != cudaSuccess) return cuda_rc(e);
-        e = launch_combine(yp, wts, pos, T, w->k, w->d_model, residual ? x : nullptr, out, s);
-    } else {
-        e = launch_ffn(x, T, *w, act, off, ptok, pslot, wts, 1, out, residual, base, L, status, s);
-    }
-    return cuda_rc(e);
+    int rc = check_device();
+    if (rc) return rc;
+    char* base = static_cast<char*>(ws);
+    const ArenaCall ac{state, layer, host_blobs};
+    return cuda_rc(layer_chain(x, T, a, act, flags, residual, out, reinterpret_cast<int32_t*>(base + L.idx),
+                               reinterpret_cast<float*>(base + L.wts), reinterpret_cast<int32_t*>(base + L.off), base,
+                               L, status, &ac, (cudaStream_t)stream));
 }
 
 }  // extern "C"

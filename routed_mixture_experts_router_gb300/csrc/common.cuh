@@ -70,6 +70,17 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Index of expert e's matrices along the expert dimension of the weight
+// arrays: e itself, or its arena slot (-1 when it has none in [0, n_slots)).
+__device__ __forceinline__ int weight_index(const int32_t* expert_slot, int n_slots, int e) {
+    if (!expert_slot) return e;
+    const int s = __ldcg(expert_slot + e);
+    return (s >= 0 && s < n_slots) ? s : -1;
+}
+
+// Entries of the weight arrays along the expert dimension.
+inline int weight_slots(const moe_layer_w& w) { return w.expert_slot ? w.n_slots : w.E; }
+
 // ---- launchers (defined in the kernel .cu files) --------------------------
 // Router (+ the bucketing too when every token fits one cluster tile and
 // `bucketed` is non-null; *bucketed then tells whether it was done).
@@ -114,5 +125,13 @@ cudaError_t launch_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t
 
 cudaError_t launch_combine(const float* ypairs, const float* wts, const int32_t* pos, int T, int k, int dm,
                            const float* residual, float* out, cudaStream_t s);
+
+// Expert arena (arena.cu).
+size_t arena_blob_bytes(const moe_layer_w& w);
+size_t arena_state_bytes(int L, int E, int S);
+cudaError_t launch_arena_init(void* state, int L, int E, int S, cudaStream_t s);
+cudaError_t launch_arena_pack_blob(const moe_layer_w& w, int layer, int e, void* blob, cudaStream_t s);
+cudaError_t launch_arena_admit(void* state, int layer, const int32_t* offsets, int P, const void* host_blobs,
+                               const moe_layer_w& arena, int32_t* slot_map, int32_t* status, cudaStream_t s);
 
 }  // namespace moe

@@ -332,6 +332,7 @@ bool decode_fused_supported(const moe_layer_w& w, int T) {
     // whole 16-byte pieces of weights and scales (K % 256 == 0) and whole
     // down items; at most 4 weight chunks per lane
     if (w.wfmt != MOE_WFMT_Q8_0 && w.wfmt != MOE_WFMT_Q4_0) return false;
+    if (w.expert_slot) return false;  // weights in expert order only
     const int rows = w.wfmt == MOE_WFMT_Q4_0 ? kDnRowsPerItemQ4 : kDnRowsPerItem;
     return T >= 1 && T <= kFuMaxT && T * w.k <= 32 && w.d_model % 256 == 0 && w.d_ff % 256 == 0 &&
            w.d_model % rows == 0 && w.d_model <= 2048 && w.d_ff <= 1024;

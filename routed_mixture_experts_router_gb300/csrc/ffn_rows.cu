@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
     const uint16_t* __restrict__ gd, const int8_t* __restrict__ uqs, const uint16_t* __restrict__ ud,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok, float* __restrict__ h,
-    float* __restrict__ out_init, int init_residual, int P) {
+    float* __restrict__ out_init, int init_residual, int P, const int32_t* __restrict__ eslot, int nslots) {
     extern __shared__ __align__(128) unsigned char gr_smem[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
     float* part = xs + (size_t)kRowsG * dm;  // [8 warps][8 pairs][gate, up][32]
 
     pdl_wait();  // routing / bucketing of this layer complete and visible
-    if (warp == 0) build_active(offsets, E, ALLTOK ? (1 << 30) : kRowsG, P, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0)
+        build_active(offsets, E, ALLTOK ? (1 << 30) : kRowsG, P, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
     if (ALLTOK) {
         for (int p = threadIdx.x; p < P; p += kThreads) {
             const int t = __ldcg(pair_tok + p);
@@ -318,7 +319,8 @@ template <int NW, int FMT>
 __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
     const float* __restrict__ h, int T, int f, int dm, int E, int k, const int8_t* __restrict__ dqs,
     const uint16_t* __restrict__ dd, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok,
-    const int32_t* __restrict__ pair_slot, const float* __restrict__ wts, int fuse, float* __restrict__ out) {
+    const int32_t* __restrict__ pair_slot, const float* __restrict__ wts, int fuse, float* __restrict__ out,
+    const int32_t* __restrict__ eslot, int nslots) {
     extern __shared__ __align__(128) unsigned char dr_smem[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
     float* part = hs + (size_t)kRowsG * f;                                             // [NW][8][32]
 
     // Offsets were complete before gate/up released this grid: Wd streams at once.
-    if (warp == 0) build_active(offsets, E, kRowsG, T * k, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0) build_active(offsets, E, kRowsG, T * k, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
     __syncthreads();
     int lo, hi;
     item_range(s_cb[s_n] * otn, &lo, &hi);
@@ -506,7 +508,7 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
     const size_t gsm = gateup_rows_smem(w.d_model, fmt);
 #define MOE_GU_ROWS(AT, FM)                                                                                       \
     launch_rows(gateup_rows_kernel<AT, FM>, kGuNW * 32, gsm, s, x, T, w.d_model, w.d_ff, w.E, w.gate.qs, w.gate.d, \
-                w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P)
+                w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P, w.expert_slot, weight_slots(w))
     cudaError_t err = fmt ? (alltok ? MOE_GU_ROWS(true, 1) : MOE_GU_ROWS(false, 1))
                           : (alltok ? MOE_GU_ROWS(true, 0) : MOE_GU_ROWS(false, 0));
 #undef MOE_GU_ROWS
@@ -515,7 +517,7 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
     const size_t dsm = down_rows_smem(w.d_ff, nw, fmt);
 #define MOE_DOWN_ROWS(NW, FM)                                                                                      \
     launch_rows(down_rows_kernel<NW, FM>, NW * 32, dsm, s, h, T, w.d_ff, w.d_model, w.E, w.k, w.down.qs, w.down.d, \
-                offsets, pair_tok, pair_slot, wts, fuse_combine, out_or_ypairs)
+                offsets, pair_tok, pair_slot, wts, fuse_combine, out_or_ypairs, w.expert_slot, weight_slots(w))
     if (fmt) {
         if (nw == 12) return MOE_DOWN_ROWS(12, 1);
         if (nw == 8) return MOE_DOWN_ROWS(8, 1);

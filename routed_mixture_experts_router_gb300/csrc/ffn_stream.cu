@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
     const uint16_t* __restrict__ gd, const int8_t* __restrict__ uqs, const uint16_t* __restrict__ ud,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok, float* __restrict__ h,
-    float* __restrict__ out_init, int init_residual, int tca, int P) {
+    float* __restrict__ out_init, int init_residual, int tca, int P, const int32_t* __restrict__ eslot,
+    int nslots) {
     extern __shared__ __align__(128) unsigned char gu_smem[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gateup_cp_kernel(
     float4* xs = reinterpret_cast<float4*>(gu_smem + (size_t)NW * NSTG * item_bytes);
 
     pdl_wait();  // routing / bucketing of this layer complete and visible
-    if (warp == 0) build_active(offsets, E, ALLTOK ? (1 << 30) : tca, P, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0)
+        build_active(offsets, E, ALLTOK ? (1 << 30) : tca, P, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
     if (ALLTOK) {
         for (int p = threadIdx.x; p < P; p += kThreads) {
             const int t = __ldcg(pair_tok + p);
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
     const float* __restrict__ h, int T, int f, int dm, int E, int k, const int8_t* __restrict__ dqs,
     const uint16_t* __restrict__ dd, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok,
     const int32_t* __restrict__ pair_slot, const float* __restrict__ wts, int fuse, float* __restrict__ out,
-    int tcp) {
+    int tcp, const int32_t* __restrict__ eslot, int nslots) {
     extern __shared__ __align__(128) unsigned char dn_smem[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
@@ -159,7 +161,8 @@ __global__ void __launch_bounds__(NW * 32, 1) down_cp_kernel(
 
     // Offsets were written two kernels back (routing/bucketing) and were
     // complete before gate/up released this grid: Wd can stream at once.
-    if (warp == 0) build_active(offsets, E, ALLP ? (1 << 30) : tcp, P, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 0)
+        build_active(offsets, E, ALLP ? (1 << 30) : tcp, P, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
     __syncthreads();
     int lo, hi;
     item_range(s_cb[s_n] * nq, &lo, &hi);
@@ -288,7 +291,7 @@ cudaError_t gateup_go(const float* x, int T, const moe_layer_w& w, const int32_t
     if (smem > kSmemCap) return cudaErrorInvalidConfiguration;
     return launch_pdl(gateup_cp_kernel<KCH, G, ALLTOK, NW, NSTG>, num_sms(), NW * 32, smem, s, x, T, dm, w.d_ff,
                       w.E, w.gate.qs, w.gate.d, w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, tca,
-                      T * w.k);
+                      T * w.k, w.expert_slot, weight_slots(w));
 }
 
 template <int KCH>
@@ -316,7 +319,8 @@ cudaError_t down_go(const float* h, int T, const moe_layer_w& w, const int32_t* 
     const size_t smem = ring + (size_t)tcp * KCH * 4 * 16 * 16;
     if (smem > kSmemCap) return cudaErrorInvalidConfiguration;
     return launch_pdl(down_cp_kernel<KCH, G, ALLP, NW, NSTG>, num_sms(), NW * 32, smem, s, h, T, f, w.d_model, w.E,
-                      w.k, w.down.qs, w.down.d, offsets, pair_tok, pair_slot, wts, fuse, out, tcp);
+                      w.k, w.down.qs, w.down.d, offsets, pair_tok, pair_slot, wts, fuse, out, tcp, w.expert_slot,
+                      weight_slots(w));
 }
 
 template <int KCH>

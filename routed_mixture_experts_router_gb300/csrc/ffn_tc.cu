@@ -73,6 +73,8 @@ struct TcParams {
     __nv_bfloat16* h;    // EPI 0: h [P][rows]
     float* out;          // EPI 1: out [T][rows] (+=); EPI 2: ypairs [P][rows]
     int32_t* status;
+    const int32_t* eslot;  // expert -> arena slot, or null (weights in expert order)
+    int nslots;
 };
 
 typedef unsigned long long f32x2;
@@ -134,17 +136,20 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 // Active experts in id order (warp-wide); buckets cut into chunks of kBN pairs.
 // Buckets clamped into [0, P] (offsets that are not a valid bucketing give
 // wrong sums, never an out-of-range pair).
+// s_act holds weight-array indices (arena slots when expert_slot is given;
+// experts without a slot are left out).
 __device__ void tc_build_active(const int32_t* offsets, int E, int P, int* s_act, int* s_beg, int* s_end, int* s_cb,
-                                int* s_n) {
+                                int* s_n, const int32_t* expert_slot, int n_slots) {
     const int lane = threadIdx.x & 31;
-    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
+    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32], wi[MOE_MAX_EXPERTS / 32];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
         const int e = 32 * j + lane;
         const int a = e < E ? __ldcg(offsets + e) : 0;
         const int b = e < E ? __ldcg(offsets + e + 1) : 0;
+        wi[j] = e < E ? weight_index(expert_slot, n_slots, e) : -1;
         lo[j] = min(max(a, 0), P);
-        hi[j] = min(max(b, lo[j]), P);
+        hi[j] = wi[j] < 0 ? lo[j] : min(max(b, lo[j]), P);
     }
     int n = 0, nc = 0;
 #pragma unroll
@@ -160,7 +165,7 @@ __device__ void tc_build_active(const int32_t* offsets, int E, int P, int* s_act
         }
         if (a) {
             const int jj = n + __popc(m & ((1u << lane) - 1u));
-            s_act[jj] = 32 * j + lane;
+            s_act[jj] = wi[j];
             s_beg[jj] = lo[j];
             s_end[jj] = hi[j];
             s_cb[jj] = nc + incl - my_c;
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tmap(&tm_b);
     }
     pdl_wait();  // bucketing and the previous stage's activations are complete
-    if (warp == 2) tc_build_active(p.offsets, p.E, p.T * p.k, s_act, s_beg, s_end, s_cb, &s_n);
+    if (warp == 2) tc_build_active(p.offsets, p.E, p.T * p.k, s_act, s_beg, s_end, s_cb, &s_n, p.eslot, p.nslots);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -588,9 +593,10 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
         if (err != cudaSuccess) return err;
     }
     CUtensorMap tg, tu, td, txb, th;
-    if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, (uint64_t)w.E * f, kBKR, kBM) ||
-        !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, (uint64_t)w.E * f, kBKR, kBM) ||
-        !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, (uint64_t)w.E * dm, kBKR, kBM) ||
+    const uint64_t ns = (uint64_t)weight_slots(w);
+    if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
+        !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
+        !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, ns * dm, kBKR, kBM) ||
         !make_tmap(&txb, xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dm, P, kBK, kBRows) ||
         !make_tmap(&th, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, P, kBK, kBRows))
         return cudaErrorInvalidValue;
@@ -608,6 +614,8 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pg.d1 = w.up.d;
     pg.h = hb;
     pg.status = status;
+    pg.eslot = w.expert_slot;
+    pg.nslots = (int)ns;
     cudaError_t err = launch_tc<2, 0>(tg, tu, txb, pg, s);
     if (err != cudaSuccess) return err;
     TcParams pd = pg;

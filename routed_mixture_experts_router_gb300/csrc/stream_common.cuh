@@ -121,18 +121,20 @@ __device__ __forceinline__ int stage_idx(int q) {
 // one round trip, through L2 (they were written by an earlier kernel, or come
 // from the caller).  Every bucket is clamped into [0, P]: offsets that are
 // not a valid bucketing give wrong sums, never an out-of-range pair.
-template <bool FROM_SMEM = false>
-__device__ void build_active(const int32_t* offsets, int E, int chunk, int P, int* s_act, int* s_beg, int* s_end,
-                             int* s_cb, int* s_n) {
+// s_act holds each active expert's index into the weight arrays (its arena
+// slot when expert_slot is given); an expert without a slot is left out.
+__device__ inline void build_active(const int32_t* offsets, int E, int chunk, int P, int* s_act, int* s_beg, int* s_end,
+                             int* s_cb, int* s_n, const int32_t* expert_slot, int n_slots) {
     const int lane = threadIdx.x & 31;
-    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32];
+    int lo[MOE_MAX_EXPERTS / 32], hi[MOE_MAX_EXPERTS / 32], wi[MOE_MAX_EXPERTS / 32];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
         const int e = 32 * j + lane;
-        const int a = e < E ? (FROM_SMEM ? offsets[e] : __ldcg(offsets + e)) : 0;
-        const int b = e < E ? (FROM_SMEM ? offsets[e + 1] : __ldcg(offsets + e + 1)) : 0;
+        const int a = e < E ? __ldcg(offsets + e) : 0;
+        const int b = e < E ? __ldcg(offsets + e + 1) : 0;
+        wi[j] = e < E ? weight_index(expert_slot, n_slots, e) : -1;
         lo[j] = min(max(a, 0), P);
-        hi[j] = min(max(b, lo[j]), P);
+        hi[j] = wi[j] < 0 ? lo[j] : min(max(b, lo[j]), P);
     }
     int n = 0, nc = 0;
 #pragma unroll
@@ -148,7 +150,7 @@ __device__ void build_active(const int32_t* offsets, int E, int chunk, int P, in
         }
         if (a) {
             const int jj = n + __popc(m & ((1u << lane) - 1u));
-            s_act[jj] = 32 * j + lane;
+            s_act[jj] = wi[j];
             s_beg[jj] = lo[j];
             s_end[jj] = hi[j];
             s_cb[jj] = nc + incl - my_c;
