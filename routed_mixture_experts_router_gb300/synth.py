@@ -57,6 +57,7 @@ class Workload:
     layers: int = 1
     residual: bool = False
     wfmt: str = "q8"  # expert weight blocks: "q8" (Q8_0, 34 B) or "q4" (Q4_0, 18 B)
+    arena_slots: int = 0  # > 0: experts served from an arena of this many HBM slots
 
 
 WORKLOADS = {
@@ -75,6 +76,11 @@ WORKLOADS = {
     "stack48_t64": Workload("stack48_t64", 5, 64, 2048, 768, 128, 8, zipf=True, layers=48, residual=True),
     "stack48_t1024": Workload("stack48_t1024", 5, 1024, 2048, 768, 128, 8, zipf=True, act="bf16", layers=48,
                               residual=True),
+    # the stack48_t1 weights served from a 1,536-slot expert arena (25% of the
+    # 6,144 experts resident, the pages' main cache configuration), a new
+    # token every step
+    "arena48_t1": Workload("arena48_t1", 5, 1, 2048, 768, 128, 8, zipf=True, layers=48, residual=True,
+                           arena_slots=1536),
     # Q4_0 experts (the 4-bit format of the pages' next stage), decode
     "decode_t1_q4": Workload("decode_t1_q4", 6, 1, 2048, 768, 128, 8, wfmt="q4"),
     "decode_t64_zipf_q4": Workload("decode_t64_zipf_q4", 7, 64, 2048, 768, 128, 8, zipf=True, wfmt="q4"),
