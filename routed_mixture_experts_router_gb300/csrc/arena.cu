@@ -335,7 +335,26 @@ __global__ void __launch_bounds__(kAdmitThreads, 1)
 
 // ------------------------------------------------------------------ copy --
 // The blobs the latest admission asked for, host memory -> arena slots.
-// Every thread keeps 4 independent 16-byte loads in flight.
+// Each blob's payload is read as one contiguous run of 16-byte pieces (all
+// threads on it, 8 independent loads in flight per thread); piece q goes to
+// the segment whose range holds it.
+constexpr int kCopyUnroll = 8;
+
+__device__ __forceinline__ uint4* copy_dst(const Segs& g, const unsigned long long (&c)[kNumSegs + 1], size_t slot,
+                                           size_t q) {
+    unsigned char* base = g.base[0];
+    unsigned long long size = g.size[0], start = 0;
+#pragma unroll
+    for (int k = 1; k < kNumSegs; ++k) {  // constant indices only: the parameters stay in registers
+        if (q >= c[k]) {
+            base = g.base[k];
+            size = g.size[k];
+            start = c[k];
+        }
+    }
+    return reinterpret_cast<uint4*>(base + slot * size) + (q - start);
+}
+
 __global__ void __launch_bounds__(256) arena_copy_kernel(const unsigned char* state, const unsigned char* host_blobs,
                                                          unsigned long long blob_bytes, Segs g) {
     const moe_arena_stats* st = reinterpret_cast<const moe_arena_stats*>(state);
@@ -344,24 +363,27 @@ __global__ void __launch_bounds__(256) arena_copy_kernel(const unsigned char* st
     const ArenaLayout A = arena_layout(st->layers, st->experts, st->slots);
     const int32_t* miss_slot = reinterpret_cast<const int32_t*>(state + A.miss_slot);
     const int32_t* miss_src = reinterpret_cast<const int32_t*>(state + A.miss_src);
+    unsigned long long c[kNumSegs + 1];  // segment starts in 16-byte pieces
+    c[0] = 0;
+#pragma unroll
+    for (int i = 0; i < kNumSegs; ++i) c[i + 1] = c[i] + g.size[i] / 16;
+    const size_t p16 = c[kNumSegs];
     const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x, nt = (size_t)gridDim.x * blockDim.x;
     for (int j = 0; j < n; ++j) {
         const size_t slot = (size_t)miss_slot[j];
-        const unsigned char* src = host_blobs + (size_t)miss_src[j] * blob_bytes + kBlobHeader;
-        for (int i = 0; i < kNumSegs; ++i) {
-            const uint4* s4 = reinterpret_cast<const uint4*>(src);
-            uint4* d4 = reinterpret_cast<uint4*>(g.base[i] + slot * g.size[i]);
-            const size_t n16 = g.size[i] / 16;
-            size_t q = tid;
-            for (; q + 3 * nt < n16; q += 4 * nt) {
-                const uint4 a = s4[q], b = s4[q + nt], c = s4[q + 2 * nt], d = s4[q + 3 * nt];
-                d4[q] = a;
-                d4[q + nt] = b;
-                d4[q + 2 * nt] = c;
-                d4[q + 3 * nt] = d;
+        const uint4* s4 = reinterpret_cast<const uint4*>(host_blobs + (size_t)miss_src[j] * blob_bytes + kBlobHeader);
+        for (size_t q0 = tid; q0 < p16; q0 += kCopyUnroll * nt) {
+            uint4 v[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const size_t q = q0 + u * nt;
+                if (q < p16) v[u] = s4[q];
             }
-            for (; q < n16; q += nt) d4[q] = s4[q];
-            src += g.size[i];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const size_t q = q0 + u * nt;
+                if (q < p16) *copy_dst(g, c, slot, q) = v[u];
+            }
         }
     }
 }
