@@ -899,6 +899,100 @@ def run_arena(args, ws, rank, local):
     return 0
 
 
+def run_ab_reuse(args, ws, rank, local):
+    """Paired A/B of the reuse-ordering traversal (MOE_FLAG_REUSE_ORDER) on a
+    prefill workload, with the protocol of
+    expxa.com/research/reuse-ordering-qualification ("Method and limits"):
+    pairs alternate AB / BA, the paired ratio candidate / baseline per pair,
+    the median paired change, and a 95% interval from 20,000 paired bootstrap
+    resamples; adopted only if the median is at least 2% faster and the
+    interval lies wholly below parity (the pages' predeclared bar)."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
+    binding.load()
+    R = args.rot
+    layers, xs, outs, wss = [], [], [], []
+    for r in range(R):
+        w = synth.make_layer(wl, r, dev)
+        layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
+                                                w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
+        del w
+        xs.append(synth.make_x(wl, dev, step=r))
+        outs.append(torch.empty(wl.T, wl.d_model, dtype=torch.float32, device=dev))
+        wss.append(binding.workspace(wl.T, layers[-1], act, 0, dev))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    for name, flags in (("A", 0), ("B", binding.MOE_FLAG_REUSE_ORDER)):
+        def call(flags=flags):
+            for r in range(R):
+                binding.layer_forward(xs[r], layers[r], act, flags, False, out=outs[r], ws=wss[r])
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        g = new_graph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        graphs[name] = g
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // (2 * args.pairs))
+
+    def trial(name):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                graphs[name].replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * R)  # ms per layer call
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        trial("A")
+        trial("B")
+    t_clk0 = time.time()
+    ta, tb = [], []
+    for i in range(args.pairs):
+        order = ("A", "B") if i % 2 == 0 else ("B", "A")
+        res = {n: trial(n) for n in order}
+        ta.append(res["A"])
+        tb.append(res["B"])
+    t_clk1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
+    ratio = np.array(tb) / np.array(ta)
+    rng = np.random.default_rng(20000)
+    boot = np.median(ratio[rng.integers(0, len(ratio), size=(20000, len(ratio)))], axis=1)
+    lo, hi = np.percentile(boot, [2.5, 97.5])
+    med = float(np.median(ratio))
+    adopt = bool(med <= 0.98 and hi < 1.0)
+    if rank == 0:
+        mb = float(np.median(tb))
+        line = {
+            "metric": METRIC, "value": wl.T / (mb / 1e3), "unit": "tokens/s", "n_gpus": ws,
+            "steps": 2 * args.pairs * reps * R, "warmup": args.warmup, "ms_per_step": mb,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if act == binding.MOE_ACT_BF16 else "f32",
+            "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
+            "config": workload_config(wl, args),
+            "ab_reuse_order": {
+                "baseline": "chunk-major units (default)", "candidate": "MOE_FLAG_REUSE_ORDER (bands of 4 row tiles)",
+                "pairs": args.pairs, "order": "alternating AB / BA", "layer_calls_per_trial": reps * R,
+                "baseline_ms_median": float(np.median(ta)), "candidate_ms_median": mb,
+                "median_paired_change": med - 1.0, "ci95": [float(lo) - 1.0, float(hi) - 1.0],
+                "bootstrap_resamples": 20000,
+                "bar": "median paired change <= -2% and the 95% interval wholly below parity",
+                "adopted": adopt},
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def sources_sha1(paths) -> str:
     """sha1 over the concatenated bytes of the given repo files (in order)."""
     import hashlib
@@ -943,6 +1037,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--slots", type=int, default=0, help="arena slots (arena workloads; 0: the workload's)")
+    ap.add_argument("--ab-reuse-order", action="store_true",
+                    help="paired A/B of the reuse-ordering traversal instead of the throughput line")
+    ap.add_argument("--pairs", type=int, default=16)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -950,6 +1047,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, ws, rank)
+        if args.ab_reuse_order:
+            return run_ab_reuse(args, ws, rank, local)
         if synth.WORKLOADS[args.workload].arena_slots > 0:
             return run_arena(args, ws, rank, local)
         if synth.WORKLOADS[args.workload].layers > 1:

@@ -98,6 +98,12 @@ extern "C" {
 
 /* ---- flags ----------------------------------------------------------- */
 #define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */
+#define MOE_FLAG_REUSE_ORDER 2   /* opt-in: the tensor-core down projection walks each expert's
+                                    work in bands of four output-row tiles across all its token
+                                    chunks (the reuse-ordering traversal of
+                                    expxa.com/research/reuse-ordering-qualification); the same
+                                    tiles with the same arithmetic in another order (bit-identical
+                                    with MOE_FLAG_DETERMINISTIC).  Off by default */
 
 /* Limits: E <= 256, k <= 32, k <= E, d_model and d_ff multiples of 32,
  * d_model <= 8192, d_ff <= 8192, T <= 65536. */

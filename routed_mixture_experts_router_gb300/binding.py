@@ -26,6 +26,7 @@ MOE_STATUS_ARENA_FULL = 4
 MOE_ACT_F32 = 0
 MOE_ACT_BF16 = 1
 MOE_FLAG_DETERMINISTIC = 1
+MOE_FLAG_REUSE_ORDER = 2
 MOE_WFMT_Q8_0 = 0
 MOE_WFMT_Q4_0 = 1
 

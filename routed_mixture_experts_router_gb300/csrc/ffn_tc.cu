@@ -47,6 +47,7 @@ constexpr int kBM = 128;      // weight rows per unit (MMA M)
 constexpr int kBKR = 128;     // int8 K per raw stage (one 128-byte row)
 constexpr int kBK = 64;       // bf16 K per operand stage (one 128-byte row)
 constexpr int kBN = 128;      // max tokens per unit (MMA N)
+constexpr int kReuseBand = 4;  // row tiles per band of the reuse-ordering traversal (down projection)
 constexpr int kBRows = 32;    // token rows per TMA box
 // Ring depths.  The raw (int8) ring is what keeps HBM busy: at a few
 // microseconds of loaded latency a sustained ~45 GB/s per SM needs ~100 KB of
@@ -75,6 +76,7 @@ struct TcParams {
     int32_t* status;
     const int32_t* eslot;  // expert -> arena slot, or null (weights in expert order)
     int nslots;
+    int band;              // unit order: 0 chunk-major, > 0 bands of that many row tiles (rows / kBM % band == 0)
 };
 
 typedef unsigned long long f32x2;
@@ -183,17 +185,34 @@ struct Unit {
     int e, m0, p0, nv, N;  // expert, first weight row, first pair, valid pairs, MMA N
 };
 
+// Unit u -> (expert, weight-row tile, token chunk).  band = 0: chunk-major
+// (a chunk's row tiles back to back, so its activations are reused at once).
+// band > 0 (the reuse-ordering traversal of
+// expxa.com/research/reuse-ordering-qualification, "What changed from the
+// first experiment"): within each expert, row tiles go in bands of `band`,
+// and a band visits every token chunk of the expert before the next band,
+// so each weight tile is reused across the expert's chunks sooner.  Each
+// expert keeps its own range of units, so both orders are a permutation of
+// the same units and every unit's arithmetic is unchanged.
 __device__ __forceinline__ Unit decode_unit(int u, int mt, const int* s_act, const int* s_beg, const int* s_end,
-                                            const int* s_cb, int n) {
-    const int g = u / mt;
+                                            const int* s_cb, int n, int band) {
+    int g = u / mt;
+    int m = u - g * mt;
     Unit U;
-    U.m0 = (u - g * mt) * kBM;
     int lo = 0, hi = n - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (s_cb[mid] <= g) lo = mid;
         else hi = mid - 1;
     }
+    if (band > 0) {
+        const int nch = s_cb[lo + 1] - s_cb[lo];
+        const int v = u - s_cb[lo] * mt;  // unit within the expert
+        const int b = v / (band * nch), r = v - b * (band * nch);
+        g = s_cb[lo] + r / band;
+        m = b * band + r % band;
+    }
+    U.m0 = m * kBM;
     U.e = s_act[lo];
     U.p0 = s_beg[lo] + (g - s_cb[lo]) * kBN;
     U.nv = min(kBN, s_end[lo] - U.p0);
@@ -275,7 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t pol = policy_evict_first();
             uint32_t rc = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
-                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
                 const int wrow = U.e * p.rows + U.m0;
                 for (int kr = 0; kr < kr_n; ++kr) {
                     const int rs = rc % kRS;
@@ -295,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             uint32_t ac = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
-                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
                 const int nb = (U.N + kBRows - 1) / kBRows;
                 for (int kr = 0; kr < kr_n && !s_abort; ++kr) {
                     for (int j = 0; j < 2; ++j) {
@@ -316,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             uint32_t ac = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
-                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+                const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
                 const int buf = uc & 1;
                 if (!tc_wait(acc_empty + buf, ((uc >> 1) & 1) ^ 1, p.status, &s_abort)) break;
                 tc_fence_after();
@@ -352,7 +371,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nbk = p.K / 32;                    // scale blocks per row
         uint32_t rc = 0, ac = 0;
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
-            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
             const size_t srow = (size_t)(U.e * p.rows + U.m0 + r) * nbk;
             // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1.
             // Four register sets on rotating stages, each refilled (for stage
@@ -421,7 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int et = ew * 32 + lane;    // pair slot staged by this thread
         uint32_t uc = 0;
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
-            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n);
+            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
             if (EPI == 1) {
                 int tok = -1;
                 float w = 0.f;
@@ -575,7 +594,7 @@ bool ffn_tc_supported(const moe_layer_w& w, int T) {
 cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                           const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                           float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
-                          cudaStream_t s) {
+                          int reuse_order, cudaStream_t s) {
     const int P = T * w.k;
     const int dm = w.d_model, f = w.d_ff;
     {
@@ -625,6 +644,7 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pd.d1 = nullptr;
     pd.h = nullptr;
     pd.out = out_or_ypairs;
+    pd.band = (reuse_order && (dm / kBM) % kReuseBand == 0) ? kReuseBand : 0;
     if (fuse_combine) return launch_tc<1, 1>(td, td, th, pd, s);
     return launch_tc<1, 2>(td, td, th, pd, s);
 }

@@ -101,3 +101,25 @@ def test_tc_repeatable_with_deterministic_flag():
     a = _run(case, flags=binding.MOE_FLAG_DETERMINISTIC)[0]
     b = _run(case, flags=binding.MOE_FLAG_DETERMINISTIC)[0]
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("shape", [
+    ("tc_reuse_multi", 512, 1024, 256, 8, 2, True),    # ~128 pairs per expert: several chunks each; 2 bands
+    ("tc_reuse_t2048", 2048, 2048, 768, 128, 8, False),  # the full geometry in one call
+], ids=lambda s: s[0])
+def test_reuse_order_traversal(shape):
+    """The band traversal of the down projection (MOE_FLAG_REUSE_ORDER) runs
+    the same tiles in another order: bit-identical with the fixed-order
+    combine, within fp32 reassociation of the atomic combine otherwise, and
+    within the bf16 tolerance of the oracle."""
+    case = make_case(_wl(*shape))
+    det = binding.MOE_FLAG_DETERMINISTIC
+    a, ia, _ = _run(case, det)
+    b, ib, _ = _run(case, det | binding.MOE_FLAG_REUSE_ORDER)
+    assert np.array_equal(ia, ib)
+    assert np.array_equal(a, b)
+    c, _, _ = _run(case, 0)
+    d, _, _ = _run(case, binding.MOE_FLAG_REUSE_ORDER)
+    assert rel_l2_max(d, c) < 1e-5
+    tokens = np.sort(np.random.default_rng(4).choice(case.wl.T, 24, replace=False))
+    _check(case, tokens=tokens, flags=binding.MOE_FLAG_REUSE_ORDER)
