@@ -114,7 +114,19 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
     unsigned char* ring = fsm + (size_t)warp * kFuNSTG * item_bytes;
     float4* act = reinterpret_cast<float4*>(fsm + (size_t)kFuNW * kFuNSTG * item_bytes);  // x, later h
 
-    // 0. activations into shared memory; combine target out = residual ? x : 0
+    // 0. this CTA's first router row into registers (it does not depend on x,
+    //    so its round trip overlaps the one of x); activations into shared
+    //    memory; combine target out = residual ? x : 0
+    constexpr int kQ = 2;  // float4 of a router row per thread: d_model <= 2048 -> d4 <= 512 <= 2 * 384
+    float4 wv[kQ];
+    if (blockIdx.x < E) {
+        const float4* wr = reinterpret_cast<const float4*>(p.Wr) + (size_t)blockIdx.x * d4;
+#pragma unroll
+        for (int u = 0; u < kQ; ++u) {
+            const int q = threadIdx.x + u * kFuThreads;
+            wv[u] = q < d4 ? __ldg(wr + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     pdl_wait();
     for (int i = threadIdx.x; i < T * d4; i += kFuThreads) {
         const int t = i / d4, q = i - t * d4;
@@ -128,13 +140,13 @@ __global__ void __launch_bounds__(kFuThreads, 1) decode_fused_kernel(FusedParams
     // 1. router logits: one expert row per CTA (all CTAs at once), its threads
     //    split K; every load of the row is in flight at once
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
-        const float4* wr = reinterpret_cast<const float4*>(p.Wr) + (size_t)e * d4;
-        constexpr int kQ = 2;  // float4 per thread: d_model <= 2048 -> d4 <= 512 <= 2 * 384
-        float4 wv[kQ];
+        if (e != blockIdx.x) {  // further rows (E > grid): loaded here
+            const float4* wr = reinterpret_cast<const float4*>(p.Wr) + (size_t)e * d4;
 #pragma unroll
-        for (int u = 0; u < kQ; ++u) {
-            const int q = threadIdx.x + u * kFuThreads;
-            wv[u] = q < d4 ? __ldg(wr + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < kQ; ++u) {
+                const int q = threadIdx.x + u * kFuThreads;
+                wv[u] = q < d4 ? __ldg(wr + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         float acc[kFuMaxT] = {0.f, 0.f};
 #pragma unroll
