@@ -42,6 +42,19 @@ def row_bytes(wl, K: int) -> int:
     return (K // 32) * (18 if wl.wfmt == "q4" else 34)
 
 
+NEAR_TIE = 1e-5  # adjacent top-(k+1) logit gap (fp64) below which a token's selection is a near-tie
+
+
+def near_tie_tokens(x: torch.Tensor, Wr: torch.Tensor, bias, k: int) -> int:
+    """Tokens whose fp64 router logits have an adjacent gap < NEAR_TIE among
+    their k+1 largest: the tokens whose selection fp32 rounding may decide."""
+    lg = x.double().cpu().numpy() @ Wr.double().cpu().numpy().T
+    if bias is not None:
+        lg = lg + bias.double().cpu().numpy()[None, :]
+    s = -np.sort(-lg, axis=1)[:, :k + 1]
+    return int(((s[:, :-1] - s[:, 1:]) < NEAR_TIE).any(axis=1).sum()) if s.shape[1] > 1 else 0
+
+
 def expert_bytes(wl) -> int:
     """HBM bytes of one expert's three quantised matrices (values + scales)."""
     return 2 * wl.d_ff * row_bytes(wl, wl.d_model) + wl.d_model * row_bytes(wl, wl.d_ff)
@@ -289,14 +302,16 @@ def run_ours(args, ws, rank, local):
     R = args.rot
     layers, xs, outs, wss = [], [], [], []
     host0 = None
+    near = 0
     for r in range(R):
         w = synth.make_layer(wl, r, dev)
         if r == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
             host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
         layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
                                                 w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
-        del w
         xs.append(synth.make_x(wl, dev, step=r))
+        near += near_tie_tokens(xs[-1], w["Wr"], w["bias"], wl.k)
+        del w
         outs.append(torch.empty(wl.T, wl.d_model, dtype=torch.float32, device=dev))
         wss.append(binding.workspace(wl.T, layers[-1], act, 0, dev))
     torch.cuda.synchronize()
@@ -574,7 +589,10 @@ def run_ours(args, ws, rank, local):
             "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
             "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
             "config": workload_config(wl, args),
-            "layer_hbm_gbs": layer_gbs, "near_ties": None,
+            "layer_hbm_gbs": layer_gbs,
+            "near_ties": {"tokens": near, "of": R * wl.T, "gap": NEAR_TIE,
+                          "note": "tokens of the rotating inputs whose fp64 top-(k+1) logits have an adjacent gap "
+                                  "below the threshold; their selection may follow fp32 rounding"},
             "separate_path_ms": {"route_and_bucket": rb_ms, "expert_ffn": ffn_ms_mean},
             "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
             "gpu_launches": launches, "gpu_launches_source": launches_src, "clocks": clocks,

@@ -102,3 +102,52 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load(str(tmp_path / "missing.so"))
     finally:
         binding._lib = saved
+
+
+def test_arena_sizes(lib):
+    """Blob bytes: a 4 KiB header page + the expert's payload, page-rounded
+    (the pages' 5,017,600 B per Q8_0 expert of the qwen3_moe geometry)."""
+    w = _layer()
+    assert lib.moe_arena_blob_bytes(ctypes.byref(w)) == 5_017_600
+    w.wfmt = binding.MOE_WFMT_Q4_0
+    assert lib.moe_arena_blob_bytes(ctypes.byref(w)) == 4096 + 2_654_208     # 648 whole pages
+    w.wfmt = 2
+    assert lib.moe_arena_blob_bytes(ctypes.byref(w)) == 0
+    n = lib.moe_arena_state_bytes(48, 128, 1536)
+    assert n >= 64 + 48 * 128 * 4 + 2 * 1536 * 4 + 2 * 128 * 4 and n % 256 == 0
+    assert lib.moe_arena_state_bytes(0, 128, 1536) == 0
+    assert lib.moe_arena_state_bytes(48, 300, 1536) == 0
+    assert lib.moe_arena_state_bytes(48, 128, 70000) == 0
+
+
+def test_arena_argument_checks(lib):
+    """Refused on the host before any device work."""
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    assert lib.moe_arena_init(None, 48, 128, 1536, None) == binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_arena_init(P(0x10010), 48, 128, 1536, None) == binding.MOE_ERR_INVALID_ARG  # not 256-aligned
+    w = _layer()
+    w.n_slots = 1536
+    assert lib.moe_arena_admit(None, 0, fake, 8, fake, ctypes.byref(w), fake, None, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_arena_admit(fake, 0, fake, 8, P(0x10008), ctypes.byref(w), fake, None, None) == \
+        binding.MOE_ERR_INVALID_ARG                                                            # blobs misaligned
+    w.n_slots = 0
+    assert lib.moe_arena_admit(fake, 0, fake, 8, fake, ctypes.byref(w), fake, None, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_arena(fake, 1, ctypes.byref(w), 0, 0, 0, P(0x20000), fake, 0, fake, fake,
+                                       1 << 20, None, None) == binding.MOE_ERR_INVALID_ARG
+    w.expert_slot = 0x30000                     # a slot map needs 1..65536 slots
+    assert lib.moe_workspace_size(4, ctypes.byref(w), 0, 0) > 0
+    assert lib.moe_layer_forward(fake, 4, ctypes.byref(w), 0, 0, 0, P(0x20000), None, None, None, fake, 1 << 30,
+                                 None, None) == binding.MOE_ERR_INVALID_ARG
+
+
+def test_q4_geometry_refused(lib):
+    """Q4_0 needs d_model % 512 == 0 (its kernels' K split): d_model 256 is
+    refused as unsupported before any device work."""
+    w = _layer(E=16, k=2, d=256, f=128)
+    w.wfmt = binding.MOE_WFMT_Q4_0
+    P = ctypes.c_void_p
+    assert lib.moe_layer_forward(P(0x10000), 4, ctypes.byref(w), 0, 0, 0, P(0x20000), None, None, None,
+                                 P(0x40000), 1 << 30, None, None) == binding.MOE_ERR_UNSUPPORTED
