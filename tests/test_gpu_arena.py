@@ -227,3 +227,29 @@ def test_arena_graph_replay():
     torch.cuda.synchronize()
     assert torch.equal(bufs[L], eager)
     assert ar.stats() == st_eager
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_arena_full_geometry(T):
+    """The qwen3_moe geometry (d_model 2048, d_ff 768, 128 experts, top-8,
+    5,017,600-byte blobs), two layers alternating: the arena layer equals the
+    resident layer bit for bit with the fixed-order combine."""
+    wl = _wl(f"arena_full_t{T}", T, 2048, 768, 128, 8)
+    L = 2
+    S = 16 if T == 1 else 128
+    layers = _layers(wl, L)
+    ar = _arena(wl, layers, S)
+    assert ar.blob_bytes == 5_017_600
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(4):
+        l = step % L
+        w, lay = layers[l]
+        x = synth.make_x(wl, "cuda", step=step)
+        got = binding.layer_forward_arena(x, ar.layer(w["Wr"], w["bias"]), ar, l, binding.MOE_ACT_F32,
+                                          binding.MOE_FLAG_DETERMINISTIC, status=status)
+        want = binding.layer_forward(x, lay, binding.MOE_ACT_F32, binding.MOE_FLAG_DETERMINISTIC)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), step
+    assert status.item() == 0
+    st = ar.stats()
+    assert st["misses"] > 0 and st["bytes_in"] == st["misses"] * 5_013_504

@@ -280,3 +280,32 @@ def test_combine_entry_point():
     o_out = oracle_layer(case, forced_idx=idx.cpu().numpy(), residual=True)[0]
     assert rel_l2_max(out.cpu().double().numpy() - case.host["x"], o_out - case.host["x"]) < TOL_F32
     assert rel_l2_max(fused.cpu().double().numpy() - case.host["x"], o_out - case.host["x"]) < TOL_F32
+
+
+@pytest.mark.parametrize("act", [binding.MOE_ACT_F32, binding.MOE_ACT_BF16], ids=["f32", "bf16"])
+def test_max_batch_t65536_sampled(act):
+    """The largest batch the ABI takes (T = 65536, 524,288 pairs) at the full
+    qwen3_moe geometry with the Zipf bias: routing of every token and the
+    bucketing bit-exact (near-ties counted), outputs of sampled tokens within
+    the path's tolerance of the oracle run with the GPU's selection."""
+    bf16 = act == binding.MOE_ACT_BF16
+    wl = synth.custom("max_t65536", wid=901, T=65536, d_model=2048, d_ff=768, E=128, k=8, zipf=True,
+                      act="bf16" if bf16 else "f32")
+    case = make_case(wl)
+    idx, wts, near = _route_and_check(case)
+    print(f"T=65536: near-tie tokens {near}")
+    off, pt, ps, pos = binding.bucket(idx, wl.E)
+    torch.cuda.synchronize()
+    check_bucket(idx.cpu().numpy(), wl.E, off.cpu().numpy(), pt.cpu().numpy(), ps.cpu().numpy(), pos.cpu().numpy())
+    idx_out = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = binding.layer_forward(case.x, case.layer, act, idx_out=idx_out, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(idx_out, idx)
+    tokens = np.sort(np.random.default_rng(65536).choice(wl.T, 32, replace=False))
+    tokens[0], tokens[-1] = 0, wl.T - 1
+    o_out = oracle_layer(case, tokens=tokens, forced_idx=idx.cpu().numpy()[tokens])[0]
+    err = rel_l2_max(out.double().cpu().numpy()[tokens], o_out)
+    print(f"T=65536 ({'bf16' if bf16 else 'f32'}): max rel L2 over 32 sampled tokens {err:.3e}")
+    assert err < (1e-2 if bf16 else TOL_F32)

@@ -113,3 +113,17 @@ def test_q4_unsupported_geometry():
     with pytest.raises(binding.MoeError) as ei:
         binding.layer_forward(case.x, case.layer)
     assert ei.value.rc == binding.MOE_ERR_UNSUPPORTED
+
+
+def test_layer_q4_prefill_t1024_sampled():
+    """Q4_0 at the full geometry and a prefill batch (lane-per-row kernels,
+    per-chunk activations, 128 experts): 48 sampled tokens against the oracle."""
+    wl = _wl("q4_t1024", 1024, 2048, 768, 128, 8, False)
+    case = make_case(wl)
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    out = binding.layer_forward(case.x, case.layer, idx_out=idx)
+    torch.cuda.synchronize()
+    tokens = np.sort(np.random.default_rng(1024).choice(wl.T, 48, replace=False))
+    o_out = oracle_layer(case, tokens=tokens, forced_idx=idx.cpu().numpy()[tokens])[0]
+    err = rel_l2_max(out.double().cpu().numpy()[tokens], o_out)
+    assert err < TOL_F32, f"max rel L2 {err:.3e}"
