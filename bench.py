@@ -1072,6 +1072,41 @@ def run_ab_reuse(args, ws, rank, local):
     return 0
 
 
+def run_read_sweep(args, local):
+    """Context for the roofline fractions: how long a one-shot, cold,
+    read-only pass over N bytes of HBM takes with a library reduction
+    (torch.sum), for N from one decode layer's bytes up to GBs.  Prints one
+    JSON line; not a throughput line of this library."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # larger than L2: evicts between passes
+    rows = []
+    for mb in (8, 21, 27, 41, 100, 270, 1000, 4000):
+        n = mb * (1 << 20) // 4
+        nb = 4 if mb <= 1000 else 1
+        bufs = [torch.randn(n, device=dev) for _ in range(nb)]
+        for b in bufs:
+            b.sum()
+        ts = []
+        for rep in range(21):
+            b = bufs[rep % nb]
+            flush.fill_(rep & 255)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            b.sum()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        t = sorted(ts)[len(ts) // 2]
+        rows.append({"mib": mb, "us": t * 1e3, "gb_s": mb * 1.048576e6 / (t / 1e3) / 1e9})
+        del bufs
+        torch.cuda.empty_cache()
+    print(json.dumps({"read_sweep": rows, "kernel": "torch.sum over fp32, cold (L2 flushed), median of 21",
+                      "peak_hbm_gbs": load_peaks()["hbm_gbs"]}), flush=True)
+    return 0
+
+
 def sources_sha1(paths) -> str:
     """sha1 over the concatenated bytes of the given repo files (in order)."""
     import hashlib
@@ -1119,6 +1154,8 @@ def main():
     ap.add_argument("--ab-reuse-order", action="store_true",
                     help="paired A/B of the reuse-ordering traversal instead of the throughput line")
     ap.add_argument("--pairs", type=int, default=16)
+    ap.add_argument("--read-sweep", action="store_true",
+                    help="time one-shot cold HBM reads of 8 MiB .. 4 GiB with a library reduction (context)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1126,6 +1163,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, ws, rank)
+        if args.read_sweep:
+            return run_read_sweep(args, local)
         if args.ab_reuse_order:
             return run_ab_reuse(args, ws, rank, local)
         if synth.WORKLOADS[args.workload].arena_slots > 0:
