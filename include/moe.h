@@ -14,10 +14,11 @@
  *            order ("compact expert grouping", expxa.com
  *            reuse-ordering-qualification, "What changed from the first
  *            experiment")
- *   experts  y = Wd (silu(Wg x) * (Wu x)), every weight Q8_0-dequantised as
- *            w = q * d (native Q8_0 weights, amalgafy.com/technical-overview,
- *            "Validated GPU foundation"; down projection K=768 -> 2048 rows,
- *            expxa.com, "What changed from the first experiment")
+ *   experts  y = Wd (silu(Wg x) * (Wu x)), every weight dequantised exactly:
+ *            Q8_0 w = q * d (native Q8_0 weights, amalgafy.com/technical-
+ *            overview, "Validated GPU foundation") or Q4_0 w = (n - 8) * d
+ *            (layout below); down projection K=768 -> 2048 rows (expxa.com,
+ *            "What changed from the first experiment")
  *   combine  out[t] = (residual ? x[t] : 0) + sum_slot w[t][slot] * y
  *            ("weighted combine", amalgafy.com/technical-overview,
  *            "Execution architecture")
@@ -86,7 +87,7 @@ extern "C" {
                                    the experts left without a slot are skipped (wrong outputs) */
 
 /* ---- expert-input precision ------------------------------------------ */
-#define MOE_ACT_F32 0  /* fp32 activations, CUDA-core Q8_0 contraction (decode) */
+#define MOE_ACT_F32 0  /* fp32 activations, CUDA-core contraction (decode) */
 #define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill); batches
                           of fewer than 128 pairs, or dimensions not multiples of 128, run the
                           fp32 path (more accurate, and memory-bound at that size anyway) */
