@@ -567,19 +567,60 @@ def run_ours(args, ws, rank, local):
         barrier(ws)
         return max_over_ranks(a.elapsed_time(b), ws, dev)
 
+    # the copies inside the captured graphs: each step's graph holds the x
+    # copy in, the layer and the out copy back, and R such steps form one
+    # graph (K / R launches for K steps; K a multiple of R)
+    def e2e_in_graph(host_x: bool):
+        if args.steps % R:
+            return None
+
+        def one(r):
+            if not host_x:
+                xs[r].copy_(xh[r], non_blocking=True)
+            binding.layer_forward(xh[r] if host_x else xs[r], layers[r], act, 0, wl.residual, out=outs[r],
+                                  ws=wss[r])
+            oh.copy_(outs[r], non_blocking=True)
+
+        g = new_graph()
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                one(r)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for r in range(R):
+                    one(r)
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            barrier(ws)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps // R):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            barrier(ws)
+        return max_over_ranks(a.elapsed_time(b), ws, dev)
+
     e2e_copy_ms, e2e_host_ms = e2e_pass(False), e2e_pass(True)
     e2e_pipe_ms = e2e_pipelined()
+    e2e_graph_ms, e2e_graph_host_ms = e2e_in_graph(False), e2e_in_graph(True)
     variants = {"x copied in, out copied back (serial on one stream)": e2e_copy_ms,
                 "x read by the kernels from the pinned host buffer, out copied back": e2e_host_ms,
                 "x copied in on a copy stream up to two steps ahead, out copied back on a third stream "
                 "(pipelined)": e2e_pipe_ms}
+    if e2e_graph_ms is not None:
+        variants[f"x copy in, layer and out copy back captured per step, {R} steps per graph launch"] = e2e_graph_ms
+        variants["layer reading x from the pinned host buffer and out copy back captured per step, "
+                 f"{R} steps per graph launch"] = e2e_graph_host_ms
     method = min(variants, key=variants.get)
     e2e_ms = variants[method]
     e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
            "d2h_bytes_per_step": xbytes, "method": method,
            "copy_in_variant_tokens_per_s": tokens / (e2e_copy_ms / 1e3),
            "host_x_variant_tokens_per_s": tokens / (e2e_host_ms / 1e3),
-           "pipelined_variant_tokens_per_s": tokens / (e2e_pipe_ms / 1e3)}
+           "pipelined_variant_tokens_per_s": tokens / (e2e_pipe_ms / 1e3),
+           "variants_tokens_per_s": {k: tokens / (v / 1e3) for k, v in variants.items()}}
 
     cpu_base = None
     if host0 is not None:
