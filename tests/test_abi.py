@@ -151,3 +151,22 @@ def test_q4_geometry_refused(lib):
     P = ctypes.c_void_p
     assert lib.moe_layer_forward(P(0x10000), 4, ctypes.byref(w), 0, 0, 0, P(0x20000), None, None, None,
                                  P(0x40000), 1 << 30, None, None) == binding.MOE_ERR_UNSUPPORTED
+
+
+def test_arena_blob_matches_printed_cache_sizes(lib):
+    """The library's blob for a Q8_0 expert of the qwen3_moe geometry
+    reproduces the pages' printed raw-cache sizes for every slot count and
+    their bytes per miss (tests/golden/expert_cache_sizes.txt)."""
+    blob = lib.moe_arena_blob_bytes(ctypes.byref(_layer()))
+    rows = [ln.split() for ln in open(os.path.join(ROOT, "tests", "golden", "expert_cache_sizes.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    checked = 0
+    for kind, *vals in rows:
+        if kind == "raw_cache_gib":
+            assert round(int(vals[0]) * blob / 2 ** 30, 2) == float(vals[1]), vals
+            checked += 1
+        elif kind == "miss_bytes":
+            per_miss = float(vals[1]) * 1e9 / int(vals[0])
+            assert abs(per_miss - blob) / blob < 3e-3, vals
+            checked += 1
+    assert checked == 6
