@@ -40,6 +40,12 @@ constexpr int kRowsG = 8;     // pairs per bucket chunk
 constexpr int kRowsNSTG = 4;  // ring stages per warp
 constexpr int kScaleBytes = kRowsFT * 4;            // a stage's scales of one matrix: 2 fp16 per row
 constexpr int kGuNW = 8;                            // gate/up warps (K = d_model split 8 ways)
+// gate/up runs two CTAs per SM (16 warps): each CTA holds chunks of at most
+// kGuG pairs and a kGuNSTG-stage ring per warp, so that its registers (128)
+// and shared memory (~113 KB) leave room for a second CTA
+constexpr int kGuG = 4;
+constexpr int kGuNSTG = 2;
+constexpr int kGuCtasPerSm = 2;
 
 // Format-dependent stage geometry.  FMT 0 (Q8_0): a row's 64 K of a stage
 // are 64 bytes (four 16-byte chunks of 16 values); FMT 1 (Q4_0): 32 bytes
@@ -110,7 +116,7 @@ __device__ __forceinline__ ulonglong2 ld_pairs(const float* v) { return *reinter
 // gives at least 4 independent FMA chains even for a single token.
 template <int NT, int FMT>
 __device__ __forceinline__ void gu_stage(const unsigned char* st, int lane, const float* xk, const int* xoff,
-                                         f32x2 (&ag)[2][kRowsG], f32x2 (&au)[2][kRowsG]) {
+                                         f32x2 (&ag)[2][kGuG], f32x2 (&au)[2][kGuG]) {
     constexpr int TB = RowsFmt<FMT>::kTileBytes;
     const uint32_t sgw = reinterpret_cast<const uint32_t*>(st + 2 * TB)[lane];
     const uint32_t suw = reinterpret_cast<const uint32_t*>(st + 2 * TB + kScaleBytes)[lane];
@@ -148,6 +154,14 @@ __device__ __forceinline__ void dn_stage(const unsigned char* st, int lane, cons
     }
 }
 
+#define MOE_GU_SWITCH(n, CALL)     \
+    switch (n) {                   \
+        case 1: CALL(1); break;    \
+        case 2: CALL(2); break;    \
+        case 3: CALL(3); break;    \
+        default: CALL(4); break;   \
+    }
+
 #define MOE_ROWS_SWITCH(n, CALL)   \
     switch (n) {                   \
         case 1: CALL(1); break;    \
@@ -166,7 +180,7 @@ __device__ __forceinline__ void dn_stage(const unsigned char* st, int lane, cons
 // ALLTOK: every token's x staged once (T <= 8); else the chunk's x is staged
 // per chunk (restaged at chunk changes).
 template <bool ALLTOK, int FMT>
-__global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
+__global__ void __launch_bounds__(kGuNW * 32, kGuCtasPerSm) gateup_rows_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
     const uint16_t* __restrict__ gd, const int8_t* __restrict__ uqs, const uint16_t* __restrict__ ud,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_tok, float* __restrict__ h,
@@ -174,20 +188,20 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
     extern __shared__ __align__(128) unsigned char gr_smem[];
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
-    __shared__ int s_tok[ALLTOK ? kMaxStagedPairs : kRowsG];
+    __shared__ int s_tok[ALLTOK ? kMaxStagedPairs : kGuG];
     constexpr int kThreads = kGuNW * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d4 = dm / 4;
     const int kw = dm / kGuNW, spi = kw / kRowsKS;
     const int ftn = f / kRowsFT;
     constexpr int kGuStage = RowsFmt<FMT>::kGuStage, TB = RowsFmt<FMT>::kTileBytes;
-    unsigned char* ring = gr_smem + (size_t)warp * kRowsNSTG * kGuStage;
-    float* xs = reinterpret_cast<float*>(gr_smem + (size_t)kGuNW * kRowsNSTG * kGuStage);  // [8 or T][dm]
-    float* part = xs + (size_t)kRowsG * dm;  // [8 warps][8 pairs][gate, up][32]
+    unsigned char* ring = gr_smem + (size_t)warp * kGuNSTG * kGuStage;
+    float* xs = reinterpret_cast<float*>(gr_smem + (size_t)kGuNW * kGuNSTG * kGuStage);  // [kGuG or T][dm]
+    float* part = xs + (size_t)kGuG * dm;  // [8 warps][kGuG pairs][gate, up][32]
 
     pdl_wait();  // routing / bucketing of this layer complete and visible
     if (warp == 0)
-        build_active(offsets, E, ALLTOK ? (1 << 30) : kRowsG, P, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
+        build_active(offsets, E, ALLTOK ? (1 << 30) : kGuG, P, s_act, s_beg, s_end, s_cb, &s_n, eslot, nslots);
     if (ALLTOK) {
         for (int p = threadIdx.x; p < P; p += kThreads) {
             const int t = __ldcg(pair_tok + p);
@@ -234,19 +248,19 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
         cp_async_commit();
     };
 #pragma unroll
-    for (int q = 0; q < kRowsNSTG - 1; ++q) issue(q, q);
+    for (int q = 0; q < kGuNSTG - 1; ++q) issue(q, q);
 
     int staged_chunk = -1;
     int n = 0, pb = 0, ft = 0, s = 0, ci = lo;
-    int xoff[kRowsG];
-    f32x2 ag[2][kRowsG], au[2][kRowsG];
+    int xoff[kGuG];
+    f32x2 ag[2][kGuG], au[2][kGuG];
     for (int q = 0; q < nst; ++q) {
         if (s == 0) {  // a new item: its pairs, and (chunked) its activations
             const int g = ci / ftn;
             ft = ci - g * ftn;
             const int a = locate(g, s_cb, s_n);
-            pb = ALLTOK ? s_beg[a] : s_beg[a] + (g - s_cb[a]) * kRowsG;
-            const int pe = ALLTOK ? s_end[a] : min(s_end[a], pb + kRowsG);
+            pb = ALLTOK ? s_beg[a] : s_beg[a] + (g - s_cb[a]) * kGuG;
+            const int pe = ALLTOK ? s_end[a] : min(s_end[a], pb + kGuG);
             n = pe - pb;
             if (!ALLTOK && g != staged_chunk) {
                 for (int j = threadIdx.x; j < n; j += kThreads) s_tok[j] = __ldcg(pair_tok + pb + j);
@@ -263,29 +277,29 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
                 staged_chunk = g;
             }
 #pragma unroll
-            for (int j = 0; j < kRowsG; ++j) {
+            for (int j = 0; j < kGuG; ++j) {
                 xoff[j] = (j < n ? (ALLTOK ? s_tok[pb + j] : j) : 0) * dm;
                 ag[0][j] = ag[1][j] = 0ull;
                 au[0][j] = au[1][j] = 0ull;
             }
         }
-        issue(q + kRowsNSTG - 1, (q + kRowsNSTG - 1) % kRowsNSTG);
-        cp_async_wait<kRowsNSTG - 1>();
+        issue(q + kGuNSTG - 1, (q + kGuNSTG - 1) % kGuNSTG);
+        cp_async_wait<kGuNSTG - 1>();
         __syncwarp();
         {
-            const unsigned char* st = ring + (size_t)(q % kRowsNSTG) * kGuStage;
+            const unsigned char* st = ring + (size_t)(q % kGuNSTG) * kGuStage;
             const float* xk = xs + warp * kw + s * kRowsKS;
 #define MOE_GU_STAGE(NT) gu_stage<NT, FMT>(st, lane, xk, xoff, ag, au)
-            MOE_ROWS_SWITCH(n, MOE_GU_STAGE)
+            MOE_GU_SWITCH(n, MOE_GU_STAGE)
 #undef MOE_GU_STAGE
         }
         __syncwarp();  // every lane done with this stage before it is refilled
         if (s == spi - 1) {  // item complete: add the warps' K slices in order
 #pragma unroll
-            for (int j = 0; j < kRowsG; ++j) {
+            for (int j = 0; j < kGuG; ++j) {
                 if (j < n) {
-                    part[((warp * kRowsG + j) * 2 + 0) * 32 + lane] = f2_sum(f2_add(ag[0][j], ag[1][j]));
-                    part[((warp * kRowsG + j) * 2 + 1) * 32 + lane] = f2_sum(f2_add(au[0][j], au[1][j]));
+                    part[((warp * kGuG + j) * 2 + 0) * 32 + lane] = f2_sum(f2_add(ag[0][j], ag[1][j]));
+                    part[((warp * kGuG + j) * 2 + 1) * 32 + lane] = f2_sum(f2_add(au[0][j], au[1][j]));
                 }
             }
             __syncthreads();
@@ -295,8 +309,8 @@ __global__ void __launch_bounds__(kGuNW * 32, 1) gateup_rows_kernel(
                     float gs = 0.f, us = 0.f;
 #pragma unroll
                     for (int w2 = 0; w2 < kGuNW; ++w2) {
-                        gs += part[((w2 * kRowsG + j) * 2 + 0) * 32 + r];
-                        us += part[((w2 * kRowsG + j) * 2 + 1) * 32 + r];
+                        gs += part[((w2 * kGuG + j) * 2 + 0) * 32 + r];
+                        us += part[((w2 * kGuG + j) * 2 + 1) * 32 + r];
                     }
                     h[(size_t)(pb + j) * f + ft * kRowsFT + r] = silu_f(gs) * us;
                 }
@@ -448,11 +462,11 @@ int rows_num_sms() {
 }
 
 template <typename K, typename... Args>
-cudaError_t launch_rows(K kern, int threads, size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_rows(K kern, int threads, size_t smem, int ctas_per_sm, cudaStream_t s, Args... args) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows_num_sms(), 1, 1);
+    cfg.gridDim = dim3(rows_num_sms() * ctas_per_sm, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -474,7 +488,7 @@ int down_rows_warps(int f) {
 
 size_t gateup_rows_smem(int dm, int fmt) {
     const size_t stage = fmt ? RowsFmt<1>::kGuStage : RowsFmt<0>::kGuStage;
-    return (size_t)kGuNW * kRowsNSTG * stage + (size_t)kRowsG * dm * 4 + (size_t)kGuNW * kRowsG * 2 * 32 * 4;
+    return (size_t)kGuNW * kGuNSTG * stage + (size_t)kGuG * dm * 4 + (size_t)kGuNW * kGuG * 2 * 32 * 4;
 }
 
 size_t down_rows_smem(int f, int nw, int fmt) {
@@ -503,11 +517,12 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
     if (T == 0) return cudaSuccess;
     const int P = T * w.k;
     float* out_init = fuse_combine ? out_or_ypairs : nullptr;
-    const bool alltok = T <= kRowsG && P <= kMaxStagedPairs;
+    const bool alltok = T <= kGuG && P <= kMaxStagedPairs;
     const int fmt = w.wfmt;
     const size_t gsm = gateup_rows_smem(w.d_model, fmt);
 #define MOE_GU_ROWS(AT, FM)                                                                                       \
-    launch_rows(gateup_rows_kernel<AT, FM>, kGuNW * 32, gsm, s, x, T, w.d_model, w.d_ff, w.E, w.gate.qs, w.gate.d, \
+    launch_rows(gateup_rows_kernel<AT, FM>, kGuNW * 32, gsm, kGuCtasPerSm, s, x, T, w.d_model, w.d_ff, w.E,       \
+                w.gate.qs, w.gate.d,                                                                             \
                 w.up.qs, w.up.d, offsets, pair_tok, h, out_init, residual, P, w.expert_slot, weight_slots(w))
     cudaError_t err = fmt ? (alltok ? MOE_GU_ROWS(true, 1) : MOE_GU_ROWS(false, 1))
                           : (alltok ? MOE_GU_ROWS(true, 0) : MOE_GU_ROWS(false, 0));
@@ -516,7 +531,7 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
     const int nw = down_rows_warps(w.d_ff);
     const size_t dsm = down_rows_smem(w.d_ff, nw, fmt);
 #define MOE_DOWN_ROWS(NW, FM)                                                                                      \
-    launch_rows(down_rows_kernel<NW, FM>, NW * 32, dsm, s, h, T, w.d_ff, w.d_model, w.E, w.k, w.down.qs, w.down.d, \
+    launch_rows(down_rows_kernel<NW, FM>, NW * 32, dsm, 1, s, h, T, w.d_ff, w.d_model, w.E, w.k, w.down.qs, w.down.d, \
                 offsets, pair_tok, pair_slot, wts, fuse_combine, out_or_ypairs, w.expert_slot, weight_slots(w))
     if (fmt) {
         if (nw == 12) return MOE_DOWN_ROWS(12, 1);
