@@ -36,8 +36,8 @@ using namespace stream;
 
 constexpr int kRowsFT = 32;   // rows per CTA item: one per lane
 constexpr int kRowsKS = 64;   // K per warp stage: two 32-wide blocks, 4 bytes of scales per row
-constexpr int kRowsG = 8;     // pairs per bucket chunk
-constexpr int kRowsNSTG = 4;  // ring stages per warp
+constexpr int kRowsG = 8;     // pairs per bucket chunk (down)
+constexpr int kRowsNSTG = 4;  // ring stages per warp (down)
 constexpr int kScaleBytes = kRowsFT * 4;            // a stage's scales of one matrix: 2 fp16 per row
 constexpr int kGuNW = 8;                            // gate/up warps (K = d_model split 8 ways)
 // gate/up runs two CTAs per SM (16 warps): each CTA holds chunks of at most
@@ -177,8 +177,9 @@ __device__ __forceinline__ void dn_stage(const unsigned char* st, int lane, cons
 // ------------------------------------------------------------------ gate/up
 // Items: (bucket chunk g, feature tile ft) with f/32 tiles per chunk.  Warp
 // w owns K range [w*dm/8, (w+1)*dm/8), SPI = dm/512 stages per item.
-// ALLTOK: every token's x staged once (T <= 8); else the chunk's x is staged
-// per chunk (restaged at chunk changes).
+// ALLTOK: every token's x staged once (T <= kGuG); else the chunk's x is
+// staged per chunk (restaged at chunk changes).  Chunks hold at most kGuG
+// pairs; two CTAs share an SM.
 template <bool ALLTOK, int FMT>
 __global__ void __launch_bounds__(kGuNW * 32, kGuCtasPerSm) gateup_rows_kernel(
     const float* __restrict__ x, int T, int dm, int f, int E, const int8_t* __restrict__ gqs,
