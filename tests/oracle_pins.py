@@ -308,6 +308,62 @@ def pin_dense_bruteforce_q4(orc):
         assert rel_l2_max(out, ro) < 1e-12, rel_l2_max(out, ro)
 
 
+def _dense_with(x_router, x_expert, w, dm, f, E, sel):
+    """Dense reference for a given selection: weights = softmax of the
+    router logits over the selection (in its order), experts fed x_expert."""
+    Wg = np.stack([np_dequant(w["gate"][e], f, dm) for e in range(E)])
+    Wu = np.stack([np_dequant(w["up"][e], f, dm) for e in range(E)])
+    Wd = np.stack([np_dequant(w["down"][e], dm, f) for e in range(E)])
+    lg = x_router @ w["Wr"].astype(np.float64).T
+    if w["bias"] is not None:
+        lg = lg + w["bias"].astype(np.float64)[None, :]
+    ls = np.take_along_axis(lg, sel, axis=1)
+    p = np.exp(ls - ls.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    G = np.einsum("efd,td->tef", Wg, x_expert)
+    U = np.einsum("efd,td->tef", Wu, x_expert)
+    Y = np.einsum("edf,tef->ted", Wd, G * expit(G) * U)
+    return np.einsum("ts,tsd->td", p, np.take_along_axis(Y, sel[:, :, None], axis=1)), p
+
+
+def pin_bf16_expert_inputs(orc):
+    """expert_input_bf16: the router reads x, the experts read
+    bf16(fp32(x)) rounded to nearest even at each step -- torch's own
+    conversions, on values placed at exact bf16 ties and on one where
+    rounding via fp32 differs from rounding the double directly."""
+    T, dm, f, E, k = 3, 64, 32, 8, 2
+    wl, x, w = tiny_layer(21, T, dm, f, E, k, zipf=True)
+    x = x.copy()
+    x[0, :4] = [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 2.0 ** -3 * (1 + 3 * 2.0 ** -8)]  # ties
+    x[1, 0] = 1 + 2.0 ** -8 + 2.0 ** -30          # via fp32: a tie -> 1.0; directly: -> 1 + 2**-7
+    xb = torch.from_numpy(x).float().bfloat16().double().numpy()
+    assert xb[0, 0] == 1.0 and xb[0, 1] == 1 + 2.0 ** -6 and xb[1, 0] == 1.0
+    out, idx, wt, _ = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k,
+                                    expert_input_bf16=True)
+    ref, rw = _dense_with(x, xb, w, dm, f, E, idx.astype(np.int64))
+    _, ridx, _, _ = dense_bruteforce(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k)
+    assert np.array_equal(idx, ridx)             # routing reads the unrounded x
+    assert np.allclose(wt, rw, rtol=1e-12, atol=1e-15)
+    assert rel_l2_max(out, ref) < 1e-12
+    plain = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k)[0]
+    assert rel_l2_max(out, plain) > 1e-6         # the rounding is applied
+
+
+def pin_forced_selection(orc):
+    """forced_idx: the given experts, in the given order, weighted by the
+    softmax of their logits (dense reference over an arbitrary selection)."""
+    T, dm, f, E, k = 4, 64, 32, 8, 3
+    wl, x, w = tiny_layer(23, T, dm, f, E, k)
+    rng = np.random.default_rng(23)
+    sel = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    out, idx, wt, _ = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, f, E, k,
+                                    forced_idx=sel)
+    ref, rw = _dense_with(x, x, w, dm, f, E, sel.astype(np.int64))
+    assert np.array_equal(idx, sel)
+    assert np.allclose(wt, rw, rtol=1e-12, atol=1e-15)
+    assert rel_l2_max(out, ref) < 1e-12
+
+
 ALL_PINS = [
     pin_half_decode,
     pin_q8_roundtrip,
@@ -323,4 +379,6 @@ ALL_PINS = [
     pin_q4_block_layout,
     pin_q4_roundtrip,
     pin_dense_bruteforce_q4,
+    pin_bf16_expert_inputs,
+    pin_forced_selection,
 ]

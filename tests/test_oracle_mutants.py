@@ -34,6 +34,9 @@ MUTANTS = {
                        "w[b * ORACLE_Q8_BLOCK_ELEMS + 2 * j] = (double)(lo - 8) * d4;\n"
                        "            w[b * ORACLE_Q8_BLOCK_ELEMS + 2 * j + 1]"),
     "q4_block_stride": ("#define ORACLE_Q4_BLOCK_BYTES 18", "#define ORACLE_Q4_BLOCK_BYTES 17"),
+    "bf16_round_half_up": ("bits = (bits + 0x7fffu + lsb) & 0xffff0000u;", "bits = (bits + 0x8000u) & 0xffff0000u;"),
+    "bf16_not_applied": ("expert_input_bf16 ? to_bf16_via_f32(xt[j]) : xt[j]", "xt[j]"),
+    "forced_selection_ignored": ("forced_idx ? forced_idx + (size_t)t * k : NULL", "NULL"),
     "router_index": ("const float* wr = Wr + (size_t)e * dm;", "const float* wr = Wr + (size_t)(E - 1 - e) * dm;"),
 }
 
