@@ -61,7 +61,7 @@ class Oracle:
         lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_dequant_q8.restype = None
         lib.oracle_dequant_q8.argtypes = [_P, _I, _I, _P]
-        lib.oracle_expert_swiglu.restype = None
+        lib.oracle_expert_swiglu.restype = _I
         lib.oracle_expert_swiglu.argtypes = [_P, _P, _P, _I, _I, _P, _P]
         lib.oracle_route.restype = _I
         lib.oracle_route.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
@@ -120,7 +120,8 @@ class Oracle:
         g, u, d = (self._c(a, np.uint8) for a in (gate, up, down))
         xv = self._c(x, np.float64)
         y = np.empty(dm, dtype=np.float64)
-        self.lib.oracle_expert_swiglu(self._p(g), self._p(u), self._p(d), dm, f, self._p(xv), self._p(y))
+        if self.lib.oracle_expert_swiglu(self._p(g), self._p(u), self._p(d), dm, f, self._p(xv), self._p(y)):
+            raise MemoryError("oracle_expert_swiglu: scratch allocation failed")
         return y
 
     def route(self, x, Wr, bias, k: int):

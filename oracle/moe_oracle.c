@@ -154,23 +154,28 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
  *   gate, up: [f][dm] (K = dm); down: [dm][f] (K = f); blocks of format fmt.
  *   x[dm] -> y[dm].
  */
-void oracle_expert_swiglu_fmt(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f, int fmt,
-                              const double* x, double* y) {
+int oracle_expert_swiglu_fmt(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f, int fmt,
+                             const double* x, double* y) {
     int kmax = dm > f ? dm : f;
     double* g = (double*)malloc(sizeof(double) * (size_t)f);
     double* u = (double*)malloc(sizeof(double) * (size_t)f);
     double* h = (double*)malloc(sizeof(double) * (size_t)f);
     double* wrow = (double*)malloc(sizeof(double) * (size_t)kmax);
-    q_matvec(gate, f, dm, fmt, x, g, wrow);
-    q_matvec(up, f, dm, fmt, x, u, wrow);
-    for (int r = 0; r < f; ++r) h[r] = silu(g[r]) * u[r];
-    q_matvec(down, dm, f, fmt, h, y, wrow);
+    int ok = g && u && h && wrow;
+    if (ok) {
+        q_matvec(gate, f, dm, fmt, x, g, wrow);
+        q_matvec(up, f, dm, fmt, x, u, wrow);
+        for (int r = 0; r < f; ++r) h[r] = silu(g[r]) * u[r];
+        q_matvec(down, dm, f, fmt, h, y, wrow);
+    }
     free(g); free(u); free(h); free(wrow);
+    return ok ? 0 : -1;
 }
 
-void oracle_expert_swiglu(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f,
-                          const double* x, double* y) {
-    oracle_expert_swiglu_fmt(gate, up, down, dm, f, 0, x, y);
+/* Returns 0, or -1 when scratch memory could not be allocated. */
+int oracle_expert_swiglu(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int dm, int f,
+                         const double* x, double* y) {
+    return oracle_expert_swiglu_fmt(gate, up, down, dm, f, 0, x, y);
 }
 
 /*
@@ -178,9 +183,10 @@ void oracle_expert_swiglu(const uint8_t* gate, const uint8_t* up, const uint8_t*
  * id, in descending-logit order; then renormalised softmax weights.
  * If forced != NULL the selection is taken from it instead (the weights are
  * still computed from the fp64 logits of the forced experts).
+ * Returns 0, or -1 when scratch memory could not be allocated.
  */
-static void route_token(const double* xt, int dm, int E, int k, const float* Wr, const float* bias,
-                        const int32_t* forced, int32_t* idx, double* w, double* logits) {
+static int route_token(const double* xt, int dm, int E, int k, const float* Wr, const float* bias,
+                       const int32_t* forced, int32_t* idx, double* w, double* logits) {
     for (int e = 0; e < E; ++e) {
         double acc = 0.0;
         const float* wr = Wr + (size_t)e * dm;
@@ -192,6 +198,7 @@ static void route_token(const double* xt, int dm, int E, int k, const float* Wr,
         for (int s = 0; s < k; ++s) idx[s] = forced[s];
     } else {
         unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+        if (!taken) return -1;
         for (int s = 0; s < k; ++s) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
@@ -208,6 +215,7 @@ static void route_token(const double* xt, int dm, int E, int k, const float* Wr,
     double den = 0.0;
     for (int s = 0; s < k; ++s) den += exp(logits[idx[s]] - lmax);
     for (int s = 0; s < k; ++s) w[s] = exp(logits[idx[s]] - lmax) / den;
+    return 0;
 }
 
 /* Round a double to fp32 (RNE) and then to bf16 (RNE): the cast the tensor-core
@@ -224,20 +232,25 @@ static double to_bf16_via_f32(double v) {
 
 /*
  * Routing only, for all tokens.  logits [T][E] may be NULL.
- * Returns 0, or -1 on invalid arguments.
+ * Returns 0, -1 on invalid arguments, -3 when scratch memory could not be
+ * allocated.
  */
 int oracle_route(int T, int dm, int E, int k, const double* x, const float* Wr, const float* bias,
                  int32_t* idx, double* w, double* logits) {
     if (T < 0 || dm <= 0 || E <= 0 || k <= 0 || k > E || !Wr || !idx || !w || (T > 0 && !x)) return -1;
+    int nomem = 0;
     int t;
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : nomem)
     for (t = 0; t < T; ++t) {
         double* lg = (double*)malloc(sizeof(double) * (size_t)E);
-        route_token(x + (size_t)t * dm, dm, E, k, Wr, bias, NULL, idx + (size_t)t * k, w + (size_t)t * k, lg);
-        if (logits) memcpy(logits + (size_t)t * E, lg, sizeof(double) * (size_t)E);
+        if (!lg) { nomem = 1; continue; }
+        if (route_token(x + (size_t)t * dm, dm, E, k, Wr, bias, NULL, idx + (size_t)t * k, w + (size_t)t * k, lg))
+            nomem = 1;
+        else if (logits)
+            memcpy(logits + (size_t)t * E, lg, sizeof(double) * (size_t)E);
         free(lg);
     }
-    return 0;
+    return nomem ? -3 : 0;
 }
 
 /*
@@ -251,6 +264,8 @@ int oracle_route(int T, int dm, int E, int k, const double* x, const float* Wr, 
  *       tensor-core path's cast; the router still reads x)
  *   forced_idx [T][k] or NULL: use this selection instead of the top-k
  *   out [T][dm]; idx [T][k]; w [T][k]; logits [T][E] or NULL
+ * Returns 0; -1 on invalid arguments; -2 when a selected expert id is out of
+ * range; -3 when scratch memory could not be allocated.
  */
 int oracle_moe_layer_fmt(int T, int dm, int f, int E, int k, const double* x, const float* Wr, const float* bias,
                          const uint8_t* gate, const uint8_t* up, const uint8_t* down, int fmt, int residual,
@@ -263,9 +278,9 @@ int oracle_moe_layer_fmt(int T, int dm, int f, int E, int k, const double* x, co
     if (fmt != 0 && fmt != 1) return -1;
     size_t gu_bytes = (size_t)f * row_bytes_of(dm, fmt);
     size_t dn_bytes = (size_t)dm * row_bytes_of(f, fmt);
-    int bad = 0;
+    int bad = 0, nomem = 0;
     int t;
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad, nomem)
     for (t = 0; t < T; ++t) {
         const double* xt = x + (size_t)t * dm;
         double* lg = (double*)malloc(sizeof(double) * (size_t)E);
@@ -274,21 +289,29 @@ int oracle_moe_layer_fmt(int T, int dm, int f, int E, int k, const double* x, co
         double* acc = (double*)calloc((size_t)dm, sizeof(double));
         int32_t* it = idx + (size_t)t * k;
         double* wt = w + (size_t)t * k;
-        route_token(xt, dm, E, k, Wr, bias, forced_idx ? forced_idx + (size_t)t * k : NULL, it, wt, lg);
+        if (!lg || !xin || !y || !acc ||
+            route_token(xt, dm, E, k, Wr, bias, forced_idx ? forced_idx + (size_t)t * k : NULL, it, wt, lg)) {
+            nomem = 1;
+            free(lg); free(xin); free(y); free(acc);
+            continue;
+        }
         if (logits) memcpy(logits + (size_t)t * E, lg, sizeof(double) * (size_t)E);
         for (int j = 0; j < dm; ++j) xin[j] = expert_input_bf16 ? to_bf16_via_f32(xt[j]) : xt[j];
         for (int s = 0; s < k; ++s) {
             int e = it[s];
             if (e < 0 || e >= E) { bad = 1; continue; }
-            oracle_expert_swiglu_fmt(gate + (size_t)e * gu_bytes, up + (size_t)e * gu_bytes,
-                                     down + (size_t)e * dn_bytes, dm, f, fmt, xin, y);
+            if (oracle_expert_swiglu_fmt(gate + (size_t)e * gu_bytes, up + (size_t)e * gu_bytes,
+                                         down + (size_t)e * dn_bytes, dm, f, fmt, xin, y)) {
+                nomem = 1;
+                continue;
+            }
             for (int o = 0; o < dm; ++o) acc[o] += wt[s] * y[o];
         }
         double* ot = out + (size_t)t * dm;
         for (int o = 0; o < dm; ++o) ot[o] = residual ? xt[o] + acc[o] : acc[o];
         free(lg); free(xin); free(y); free(acc);
     }
-    return bad ? -2 : 0;
+    return nomem ? -3 : bad ? -2 : 0;
 }
 
 /* The layer with Q8_0 experts. */
@@ -307,12 +330,14 @@ int oracle_moe_layer(int T, int dm, int f, int E, int k, const double* x, const 
  *   pair_tok, pair_slot [T*k]: the pairs in bucket order; within one expert,
  *       ascending (token, slot)
  *   pos [T*k]: pos[t*k + s] = bucket position of pair (t, s)
- * Returns 0, or -1 if an id is out of range (outputs then undefined).
+ * Returns 0, -1 if an id is out of range (outputs then undefined), or -3 when
+ * scratch memory could not be allocated.
  */
 int oracle_bucket(const int32_t* idx, int T, int k, int E, int32_t* off, int32_t* pair_tok, int32_t* pair_slot,
                   int32_t* pos) {
     if (T < 0 || k <= 0 || E <= 0) return -1;
     int32_t* cnt = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    if (!cnt) return -3;
     for (long p = 0; p < (long)T * k; ++p) {
         int e = idx[p];
         if (e < 0 || e >= E) { free(cnt); return -1; }

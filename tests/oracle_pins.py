@@ -364,6 +364,48 @@ def pin_forced_selection(orc):
     assert rel_l2_max(out, ref) < 1e-12
 
 
+def np_route(x, Wr, bias, k):
+    """Independent router reference in numpy: fp64 logits, top-k by (logit
+    descending, id ascending), full softmax over every expert masked to the
+    selection and renormalised."""
+    logits = x @ Wr.astype(np.float64).T
+    if bias is not None:
+        logits = logits + bias.astype(np.float64)[None, :]
+    T, E = logits.shape
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    sel = np.lexsort((ids, -logits), axis=-1)[:, :k]
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    ps = np.take_along_axis(p, sel, axis=1)
+    return sel.astype(np.int32), ps / ps.sum(axis=1, keepdims=True), logits
+
+
+def pin_route_standalone(orc):
+    """The routing-only entry (every token's logits, selection and weights,
+    written at its own stride) equals the numpy router reference and the
+    routing the whole-layer entry reports, on several token counts, with and
+    without the Zipf bias, k = E, and a zero token whose logits all tie."""
+    for seed, (T, dm, E, k, zipf) in enumerate([
+        (4, 256, 16, 2, False),     # the tiny workload's geometry
+        (9, 64, 32, 4, True),
+        (5, 32, 6, 6, False),       # k == E
+        (37, 128, 128, 8, True),    # full expert count and top-8, many tokens
+        (3, 64, 8, 3, False),
+    ]):
+        wl, x, w = tiny_layer(40 + seed, T, dm, 32, E, k, zipf)
+        if T >= 3 and not zipf:
+            x[1] = 0.0  # all logits exactly 0: the lowest ids, equal weights
+        idx, wt, logits = orc.route(x, w["Wr"], w["bias"], k)
+        ridx, rw, rl = np_route(x, w["Wr"], w["bias"], k)
+        assert np.allclose(logits, rl, rtol=0, atol=1e-12), seed
+        assert np.array_equal(idx, ridx), (seed, idx, ridx)
+        assert np.allclose(wt, rw, rtol=1e-12, atol=1e-15), seed
+        _, lidx, lw, ll = orc.moe_layer(x, w["Wr"], w["bias"], w["gate"], w["up"], w["down"], dm, 32, E, k)
+        assert np.array_equal(idx, lidx) and np.array_equal(wt, lw) and np.array_equal(logits, ll), seed
+        if T >= 3 and not zipf:
+            assert np.array_equal(idx[1], np.arange(k)) and np.all(wt[1] == 1.0 / k)
+
+
 ALL_PINS = [
     pin_half_decode,
     pin_q8_roundtrip,
@@ -381,4 +423,5 @@ ALL_PINS = [
     pin_dense_bruteforce_q4,
     pin_bf16_expert_inputs,
     pin_forced_selection,
+    pin_route_standalone,
 ]

@@ -38,6 +38,13 @@ MUTANTS = {
     "bf16_not_applied": ("expert_input_bf16 ? to_bf16_via_f32(xt[j]) : xt[j]", "xt[j]"),
     "forced_selection_ignored": ("forced_idx ? forced_idx + (size_t)t * k : NULL", "NULL"),
     "router_index": ("const float* wr = Wr + (size_t)e * dm;", "const float* wr = Wr + (size_t)(E - 1 - e) * dm;"),
+    "route_idx_stride": ("NULL, idx + (size_t)t * k, w + (size_t)t * k, lg)",
+                         "NULL, idx + (size_t)t, w + (size_t)t * k, lg)"),
+    "route_weight_stride": ("NULL, idx + (size_t)t * k, w + (size_t)t * k, lg)",
+                            "NULL, idx + (size_t)t * k, w + (size_t)t, lg)"),
+    "route_logits_stride": ("            memcpy(logits + (size_t)t * E, lg, sizeof(double) * (size_t)E);\n        free(lg);",
+                            "            memcpy(logits + (size_t)t * k, lg, sizeof(double) * (size_t)E);\n        free(lg);"),
+    "route_token_offset": ("route_token(x + (size_t)t * dm, dm,", "route_token(x + (size_t)t * E, dm,"),
 }
 
 
