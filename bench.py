@@ -160,15 +160,39 @@ class ClockSampler:
 
 
 def cpu_info():
-    model = "unknown"
+    """(CPU model, logical cores).  x86 /proc/cpuinfo has "model name"; Arm
+    (e.g. NVIDIA Grace) has only implementer / part codes there, so lscpu's
+    "Model name" is tried first, then the Arm codes are named."""
+    model = None
     try:
-        for ln in open("/proc/cpuinfo"):
-            if ln.lower().startswith(("model name", "cpu model")):
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
                 model = ln.split(":", 1)[1].strip()
                 break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    impl = part = None
+    try:
+        for ln in open("/proc/cpuinfo"):
+            key = ln.split(":", 1)[0].strip().lower()
+            if model is None and key in ("model name", "cpu model"):
+                model = ln.split(":", 1)[1].strip()
+            elif key == "cpu implementer" and impl is None:
+                impl = ln.split(":", 1)[1].strip()
+            elif key == "cpu part" and part is None:
+                part = ln.split(":", 1)[1].strip()
     except OSError:
         pass
-    return model, os.cpu_count()
+    arm_parts = {("0x41", "0xd4f"): "Arm Neoverse V2 (NVIDIA Grace)", ("0x41", "0xd40"): "Arm Neoverse V1",
+                 ("0x41", "0xd0c"): "Arm Neoverse N1"}
+    if impl is not None and part is not None:
+        named = arm_parts.get((impl.lower(), part.lower()), f"Arm CPU implementer {impl} part {part}")
+        if model is None or model.lower() in ("-", "unknown"):
+            model = named
+        elif named not in model:
+            model = f"{model} ({named})"
+    return model or "unknown", os.cpu_count()
 
 
 # ----------------------------------------------------------- CPU oracle ----
@@ -200,7 +224,7 @@ def oracle_tokens_per_s(wl, layer_host, x_all: np.ndarray, budget_s: float = 12.
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[args.workload or "decode_t1"]
     w = synth.make_layer(wl, 0, "cpu")
     host = {k: (None if v is None else v.numpy()) for k, v in w.items()}
     import oracle
@@ -282,32 +306,67 @@ def graph_kernel_nodes(g):
 
 
 
-def workload_config(wl, args):
-    return {"workload": f"{wl.name}: one MoE layer, T={wl.T}, d_model={wl.d_model}, d_ff={wl.d_ff}, E={wl.E}, "
-                        f"top-{wl.k}, {fmt_name(wl)} SwiGLU experts, {wl.act} activations",
-            "tokens_per_step": wl.T, "layers_rotated": args.rot,
-            "l2": f"inputs larger than L2: steps rotate over {args.rot} seeded layers "
-                  f"({args.rot} x {wl.E} experts x {expert_bytes(wl)} B resident)",
+def workload_config(wl, args, rot=None):
+    rot = args.rot if rot is None else rot
+    mb = f" as {wl.T // wl.microbatch} microbatches of {wl.microbatch} tokens (one layer call each)" \
+        if wl.microbatch else ""
+    return {"workload": f"{wl.name}: one MoE layer, T={wl.T}{mb}, d_model={wl.d_model}, d_ff={wl.d_ff}, E={wl.E}, "
+                        f"top-{wl.k}, {fmt_name(wl)} SwiGLU experts, {wl.act} expert inputs"
+                        f"{', Zipf router bias' if wl.zipf else ''}",
+            "tokens_per_step": wl.T, "layers_rotated": rot,
+            "l2": f"inputs larger than L2: steps rotate over {rot} seeded layers "
+                  f"({rot} x {wl.E} experts x {expert_bytes(wl)} B resident)",
             "parallelism": f"replicas x{args.gpus}",
-            "graph": f"the layer forward captured as a CUDA graph per step; the K steps timed as one graph launch "
-                     f"per step and as one launch per {args.rot} rotating steps, the faster reported (timed_loop)"}
+            "graph": "the layer forward captured as a CUDA graph per step; the K steps timed as one graph launch "
+                     f"per step and as one launch per {rot} rotating steps (K mod {rot} steps as single graphs), "
+                     "the faster reported (timed_loop)"}
+
+
+def expert_path_name(wl, tc_path: bool) -> str:
+    if tc_path:
+        return "moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)"
+    return f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"
+
+
+def time_loops(stream, graphs, g_all, steps: int):
+    """The K steps timed two ways on `stream`: one graph launch per step, and
+    (when there is a rotation graph) one launch per rotation with the K mod R
+    leftover steps as single graphs.  Returns {name: ms}."""
+    R = len(graphs)
+    loops = {}
+    names = ["per_step_graphs"] + (["one_graph_per_rotation"] if g_all is not None and steps >= R else [])
+    for name in names:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if name == "one_graph_per_rotation":
+            for _ in range(steps // R):
+                g_all.replay()
+            for i in range(steps - (steps // R) * R):
+                graphs[i].replay()
+        else:
+            for i in range(steps):
+                graphs[i % R].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        loops[name] = e0.elapsed_time(e1)
+    return loops
 
 
 # ------------------------------------------------------------------ ours ----
-def run_ours(args, ws, rank, local):
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    wl = synth.WORKLOADS[args.workload]
+def measure_layer(wl, args, ws, rank, dev, sampler, rot: int, steps: int, warmup: int, cpu_budget: float,
+                  e2e_variants: bool = False):
+    """One MoE layer per step (T tokens, or T / microbatch layer calls), the
+    steps rotating over `rot` seeded layers.  Returns the bench record."""
     act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
-    tc_path = act == binding.MOE_ACT_BF16 and wl.T * wl.k >= 128
-    binding.load()
-    R = args.rot
+    mb = wl.microbatch or wl.T
+    tc_path = act == binding.MOE_ACT_BF16 and mb * wl.k >= 128
+    R = rot
     layers, xs, outs, wss = [], [], [], []
     host0 = None
     near = 0
     for r in range(R):
         w = synth.make_layer(wl, r, dev)
-        if r == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        if r == 0 and rank == 0 and ws == 1 and cpu_budget > 0:
             host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
         layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
                                                 w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
@@ -315,34 +374,38 @@ def run_ours(args, ws, rank, local):
         near += near_tie_tokens(xs[-1], w["Wr"], w["bias"], wl.k)
         del w
         outs.append(torch.empty(wl.T, wl.d_model, dtype=torch.float32, device=dev))
-        wss.append(binding.workspace(wl.T, layers[-1], act, 0, dev))
+        wss.append(binding.workspace(mb, layers[-1], act, 0, dev))
     torch.cuda.synchronize()
-    P = wl.T * wl.k
-    # split buffers for the per-kernel (expert FFN) timing pass
-    idxs = [torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev) for _ in range(R)]
-    wtss = [torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev) for _ in range(R)]
+    P = mb * wl.k
+    nmb = wl.T // mb
+    # split buffers for the per-kernel (expert FFN) timing pass, first microbatch
+    idxs = [torch.empty(mb, wl.k, dtype=torch.int32, device=dev) for _ in range(R)]
+    wtss = [torch.empty(mb, wl.k, dtype=torch.float32, device=dev) for _ in range(R)]
     offs = [torch.empty(wl.E + 1, dtype=torch.int32, device=dev) for _ in range(R)]
     pts = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
     pss = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
     poss = [torch.empty(P, dtype=torch.int32, device=dev) for _ in range(R)]
-    outs2 = [torch.empty_like(o) for o in outs]
+    outs2 = [torch.empty(mb, wl.d_model, dtype=torch.float32, device=dev) for _ in range(R)]
 
     stream = torch.cuda.Stream(device=dev)
     L = binding.load()
     st = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
 
-    def step_call(r):
-        binding.layer_forward(xs[r], layers[r], act, 0, wl.residual, out=outs[r], ws=wss[r])
+    def step_call(r, x=None):
+        x = xs[r] if x is None else x
+        for m in range(nmb):
+            binding.layer_forward(x[m * mb:(m + 1) * mb], layers[r], act, 0, wl.residual,
+                                  out=outs[r][m * mb:(m + 1) * mb], ws=wss[r])
 
     def rb_call(r):
-        binding._check("moe_route", L.moe_route(binding._ptr(xs[r]), wl.T, layers[r].ref(), binding._ptr(idxs[r]),
+        binding._check("moe_route", L.moe_route(binding._ptr(xs[r]), mb, layers[r].ref(), binding._ptr(idxs[r]),
                                                 binding._ptr(wtss[r]), binding.ctypes.c_void_p(st())))
-        binding._check("moe_bucket", L.moe_bucket(binding._ptr(idxs[r]), wl.T, wl.k, wl.E, binding._ptr(offs[r]),
+        binding._check("moe_bucket", L.moe_bucket(binding._ptr(idxs[r]), mb, wl.k, wl.E, binding._ptr(offs[r]),
                                                   binding._ptr(pts[r]), binding._ptr(pss[r]), binding._ptr(poss[r]),
                                                   None, binding.ctypes.c_void_p(st())))
 
     def ffn_call(r):
-        binding.expert_ffn_q8(xs[r], layers[r], offs[r], pts[r], pss[r], wtss[r], act, True, wl.residual,
+        binding.expert_ffn_q8(xs[r][:mb], layers[r], offs[r], pts[r], pss[r], wtss[r], act, True, wl.residual,
                               ws=wss[r], out=outs2[r])
 
     # eager warm-up (also sets kernel attributes outside capture), then capture
@@ -360,90 +423,59 @@ def run_ours(args, ws, rank, local):
                 fn(r)
             lst.append(g)
     torch.cuda.synchronize()
-    # the R rotating steps back to back in one graph: the timed loop replays it
-    # K / R times (K steps exactly), so graph launches do not gap the steps
-    g_all = None
-    if args.steps % R == 0:
-        g_all = new_graph()
-        with torch.cuda.graph(g_all, stream=stream):
-            for r in range(R):
-                step_call(r)
-        torch.cuda.synchronize()
+    g_all = new_graph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for r in range(R):
+            step_call(r)
+    torch.cuda.synchronize()
 
-    # kernels per step, read back from the captured step graphs
     per_step = [graph_kernel_nodes(g) for g in g_step]
     if all(v is not None for v in per_step):
-        launches = int(sum(per_step[i % R] for i in range(args.steps)))
+        launches = int(sum(per_step[i % R] for i in range(steps)))
         launches_src = "kernel nodes of the captured step graphs"
     else:
-        launches = None
-        launches_src = "graph introspection unavailable"
+        launches, launches_src = None, "graph introspection unavailable"
 
-    # distinct experts per rotation slot (for the algorithmic bytes)
-    n_active = []
-    for r in range(R):
-        o = offs[r].cpu().numpy()
-        n_active.append(int((np.diff(o) > 0).sum()))
+    # distinct experts per rotation slot and microbatch (for the algorithmic bytes)
     xbytes = wl.T * wl.d_model * 4
-    ffn_bytes = [n * expert_bytes(wl) + 2 * xbytes for n in n_active]        # weights + x in + out
-    step_bytes = [b + wl.E * wl.d_model * 4 + (wl.E * 4 if wl.zipf else 0) for b in ffn_bytes]  # + router
+    n_active = [int((np.diff(offs[r].cpu().numpy()) > 0).sum()) for r in range(R)]
+    ffn_bytes = [n * expert_bytes(wl) + 2 * mb * wl.d_model * 4 for n in n_active]  # weights + x in + out
+    step_bytes = [nmb * (b + wl.E * wl.d_model * 4 + (wl.E * 4 if wl.zipf else 0)) for b in ffn_bytes]
 
-    sampler = ClockSampler(local)
-    sampler.start()
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
+        for i in range(warmup):
             g_step[i % R].replay()
         torch.cuda.synchronize()
-        # soak: keep the GPU busy ~1 s so the sampled clocks reflect load
         t_soak = time.time()
         i = 0
         while time.time() - t_soak < args.soak:
-            for _ in range(200):
+            for _ in range(20):
                 g_step[i % R].replay()
                 i += 1
             torch.cuda.synchronize()
         t_clk0 = time.time()
         barrier(ws)
         torch.cuda.synchronize()
-        # the K steps timed two ways: one graph launch per step, and (K a
-        # multiple of R) one launch per R steps; the faster is reported
-        loops = {}
-        for name in (("per_step_graphs", "one_graph_per_rotation") if g_all is not None else ("per_step_graphs",)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if name == "one_graph_per_rotation":
-                for _ in range(args.steps // R):
-                    g_all.replay()
-            else:
-                for i in range(args.steps):
-                    g_step[i % R].replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            loops[name] = e0.elapsed_time(e1)
+        loops = time_loops(stream, g_step, g_all, steps)
         barrier(ws)
         t_clk1 = time.time()
     timing = min(loops, key=loops.get)
     ms_local = loops[timing]
-    sampler.stop()
     clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
     ms = max_over_ranks(ms_local, ws, dev)
-    tokens = args.steps * wl.T * ws
-    value = job_rate(args.steps, wl.T, ws, ms)
+    value = job_rate(steps, wl.T, ws, ms)
 
     # One kernel node per step means the whole layer ran as the fused
     # single-launch decode kernel: that kernel is the roofline subject, timed
-    # over the timed loop (each step: the kernel and the 8-byte memset of its
-    # barrier words before it).
-    fused_step = all(v == 1 for v in per_step if v is not None) and per_step[0] is not None
-    if fused_step:
-        fused_ms = ms_local / args.steps
+    # over the timed loop (each step: the kernel and the memset before it).
+    fused_step = per_step[0] is not None and all(v == 1 for v in per_step) and nmb == 1
 
     # per-kernel pass: events around the expert FFN (gate/up + down) on the launch stream
     with torch.cuda.stream(stream):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         torch.cuda.synchronize()
-        for i in range(args.steps):
+        for i in range(steps):
             r = i % R
             evs[i][2].record(stream)
             g_rb[r].replay()
@@ -451,29 +483,30 @@ def run_ours(args, ws, rank, local):
             g_ffn[r].replay()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
-    ffn_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    ffn_ms_mean = float(np.mean([a.elapsed_time(b) for a, b, _ in evs]))
     rb_ms = float(np.mean([c.elapsed_time(a) for a, _, c in evs]))
-    ffn_ms_mean = float(np.mean(ffn_ms))
-    ffn_alg = float(np.mean([ffn_bytes[i % R] for i in range(args.steps)]))
+    ffn_alg = float(np.mean([ffn_bytes[i % R] for i in range(steps)]))
     peaks = load_peaks()
     achieved = ffn_alg / (ffn_ms_mean / 1e3) / 1e9
-    flops = 2.0 * wl.T * wl.k * 3 * wl.d_model * wl.d_ff            # expert contractions per FFN call
-    roofline = {"kernel": ("moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)" if tc_path
-                           else f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"),
+    flops = 2.0 * mb * wl.k * 3 * wl.d_model * wl.d_ff            # expert contractions per FFN call
+    roofline = {"kernel": expert_path_name(wl, tc_path),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": ffn_alg, "launch_ms": ffn_ms_mean,
+                "launch_ms_note": f"CUDA events around the expert FFN call on its stream, mean of {steps}"
+                                  + (f" (first microbatch of {mb} tokens)" if nmb > 1 else ""),
                 "traffic": load_traffic(f"moe_expert_ffn_q8 {wl.name}")}
     if fused_step:
-        step_alg0 = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
+        fused_ms = ms_local / steps
+        step_alg0 = float(np.mean([step_bytes[i % R] for i in range(steps)]))
         fa = step_alg0 / (fused_ms / 1e3) / 1e9
-        roofline = {"kernel": f"decode_fused_kernel (whole layer: router, top-k, bucketing, {fmt_name(wl)} gate/up + down, "
-                              "combine; one cooperative launch)",
+        roofline = {"kernel": f"decode_fused_kernel (whole layer: router, top-k, bucketing, {fmt_name(wl)} "
+                              "gate/up + down, combine; one cooperative launch)",
                     "bound": "hbm", "achieved": fa, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": fa / peaks["hbm_gbs"], "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": step_alg0, "launch_ms": fused_ms,
-                    "launch_ms_note": "per step of the timed loop: the kernel plus the 8-byte memset of its "
-                                      "barrier words (the step graph's two nodes)",
+                    "launch_ms_note": "per step of the timed loop (CUDA events on the launch stream): the kernel "
+                                      "plus the memset of its synchronisation words (the step graph's two nodes)",
                     "traffic": load_traffic(f"decode_fused_kernel {wl.name}"),
                     "expert_ffn_three_kernel_path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
                                                      "launch_ms": ffn_ms_mean}}
@@ -482,194 +515,122 @@ def run_ours(args, ws, rank, local):
         roofline["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                               "frac": tf / peaks["bf16_tflops"], "flops_per_launch": flops,
                               "note": "arithmetic intensity below the bf16 ridge: HBM binds"}
-    step_alg = float(np.mean([step_bytes[i % R] for i in range(args.steps)]))
-    layer_gbs = step_alg / (ms_local / args.steps / 1e3) / 1e9
+    step_alg = float(np.mean([step_bytes[i % R] for i in range(steps)]))
+    layer_gbs = step_alg / (ms_local / steps / 1e3) / 1e9
 
-    # end to end through the C ABI from pinned host buffers, two ways:
-    # (a) copy x in, run the layer, copy out back; (b) the layer reads x straight
-    # from the pinned host buffer (GB300: the host memory is coherent with the
-    # GPU over NVLink-C2C, and the kernels touch x only with plain loads), and
-    # out is copied back.  Either way every step moves x host -> device and
-    # out device -> host inside the timed region.
+    # end to end through the C ABI: every step copies x in from pinned host
+    # memory on the layer's stream, runs the layer and copies out back, in
+    # that order on one stream (the fixed protocol reported as e2e.value)
     xh = [x.cpu().pin_memory() for x in xs]
     oh = torch.empty(wl.T, wl.d_model, dtype=torch.float32).pin_memory()
-    g_host = []
-    with torch.cuda.stream(stream):
-        for r in range(R):
-            binding.layer_forward(xh[r], layers[r], act, 0, wl.residual, out=outs[r], ws=wss[r])
-        torch.cuda.synchronize()
-        for r in range(R):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                binding.layer_forward(xh[r], layers[r], act, 0, wl.residual, out=outs[r], ws=wss[r])
-            g_host.append(g)
-    torch.cuda.synchronize()
 
-    def e2e_pass(host_x: bool) -> float:
+    def e2e_serial() -> float:
         with torch.cuda.stream(stream):
-            for i in range(min(args.warmup, 10)):
-                (g_host if host_x else g_step)[i % R].replay()
+            for i in range(min(warmup, 10)):
+                xs[i % R].copy_(xh[i % R], non_blocking=True)
+                g_step[i % R].replay()
+                oh.copy_(outs[i % R], non_blocking=True)
             torch.cuda.synchronize()
             barrier(ws)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for i in range(args.steps):
+            for i in range(steps):
                 r = i % R
-                if host_x:
-                    g_host[r].replay()
-                else:
-                    xs[r].copy_(xh[r], non_blocking=True)
-                    g_step[r].replay()
+                xs[r].copy_(xh[r], non_blocking=True)
+                g_step[r].replay()
                 oh.copy_(outs[r], non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize()
             barrier(ws)
         return max_over_ranks(a.elapsed_time(b), ws, dev)
 
-    # pipelined: step i+1's x copy (own stream) overlaps step i's layer, at
-    # most two steps ahead of it; out of step i is read back on a third
-    # stream while step i+1 runs (the out buffer of step i is reused R steps
-    # later, after its read-back has finished)
-    cs = torch.cuda.Stream(device=dev)
-    ds = torch.cuda.Stream(device=dev)
-
-    def e2e_pipelined() -> float:
-        ready = [torch.cuda.Event() for _ in range(R)]
-        done = [torch.cuda.Event() for _ in range(R)]
-        read = [torch.cuda.Event() for _ in range(R)]
-        torch.cuda.synchronize()
-        barrier(ws)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        cs.wait_stream(stream)
-        ds.wait_stream(stream)
-        for i in range(args.steps):
-            r = i % R
-            with torch.cuda.stream(cs):
-                if i >= 2:
-                    cs.wait_event(done[(i - 2) % R])     # at most two steps ahead
-                xs[r].copy_(xh[r], non_blocking=True)
-                ready[r].record(cs)
-            stream.wait_event(ready[r])
-            if i >= R:
-                stream.wait_event(read[r])               # out[r] of step i-R read back
-            with torch.cuda.stream(stream):
-                g_step[r].replay()
-            done[r].record(stream)
-            with torch.cuda.stream(ds):
-                ds.wait_event(done[r])
-                oh.copy_(outs[r], non_blocking=True)
-                read[r].record(ds)
-        stream.wait_stream(cs)
-        stream.wait_stream(ds)
-        b.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-        return max_over_ranks(a.elapsed_time(b), ws, dev)
-
-    # the copies inside the captured graphs: each step's graph holds the x
-    # copy in, the layer and the out copy back, and R such steps form one
-    # graph (K / R launches for K steps; K a multiple of R)
-    def e2e_in_graph(host_x: bool):
-        if args.steps % R:
-            return None
-
-        def one(r):
-            if not host_x:
-                xs[r].copy_(xh[r], non_blocking=True)
-            binding.layer_forward(xh[r] if host_x else xs[r], layers[r], act, 0, wl.residual, out=outs[r],
-                                  ws=wss[r])
-            oh.copy_(outs[r], non_blocking=True)
-
-        g = new_graph()
+    tokens = steps * wl.T * ws
+    e2e_ms = e2e_serial()
+    e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
+           "d2h_bytes_per_step": xbytes,
+           "method": "fixed protocol: x copied in from pinned host memory (cudaMemcpyAsync on the layer's stream), "
+                     "the layer's step graph, out copied back to pinned host memory; serial on one stream"}
+    if e2e_variants:
+        # context only: the layer reading x straight from the pinned host
+        # buffer (GB300's host memory is coherent with the GPU over NVLink-C2C)
+        g_host = []
         with torch.cuda.stream(stream):
             for r in range(R):
-                one(r)
+                step_call(r, xh[r])
             torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(R):
-                    one(r)
-            for _ in range(2):
-                g.replay()
+            for r in range(R):
+                g = new_graph()
+                with torch.cuda.graph(g, stream=stream):
+                    step_call(r, xh[r])
+                g_host.append(g)
+            torch.cuda.synchronize()
+            for i in range(min(warmup, 10)):
+                g_host[i % R].replay()
             torch.cuda.synchronize()
             barrier(ws)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(args.steps // R):
-                g.replay()
+            for i in range(steps):
+                g_host[i % R].replay()
+                oh.copy_(outs[i % R], non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize()
             barrier(ws)
-        return max_over_ranks(a.elapsed_time(b), ws, dev)
-
-    e2e_copy_ms, e2e_host_ms = e2e_pass(False), e2e_pass(True)
-    e2e_pipe_ms = e2e_pipelined()
-    e2e_graph_ms, e2e_graph_host_ms = e2e_in_graph(False), e2e_in_graph(True)
-    variants = {"x copied in, out copied back (serial on one stream)": e2e_copy_ms,
-                "x read by the kernels from the pinned host buffer, out copied back": e2e_host_ms,
-                "x copied in on a copy stream up to two steps ahead, out copied back on a third stream "
-                "(pipelined)": e2e_pipe_ms}
-    if e2e_graph_ms is not None:
-        variants[f"x copy in, layer and out copy back captured per step, {R} steps per graph launch"] = e2e_graph_ms
-        variants["layer reading x from the pinned host buffer and out copy back captured per step, "
-                 f"{R} steps per graph launch"] = e2e_graph_host_ms
-    method = min(variants, key=variants.get)
-    e2e_ms = variants[method]
-    e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
-           "d2h_bytes_per_step": xbytes, "method": method,
-           "copy_in_variant_tokens_per_s": tokens / (e2e_copy_ms / 1e3),
-           "host_x_variant_tokens_per_s": tokens / (e2e_host_ms / 1e3),
-           "pipelined_variant_tokens_per_s": tokens / (e2e_pipe_ms / 1e3),
-           "variants_tokens_per_s": {k: tokens / (v / 1e3) for k, v in variants.items()}}
+        hx_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
+        e2e["context_variants_tokens_per_s"] = {
+            "layer reads x from the pinned host buffer, out copied back": tokens / (hx_ms / 1e3)}
 
     cpu_base = None
     if host0 is not None:
         xa = synth.make_x(wl, "cpu", step=1000, T=256).double().numpy()
-        tps, done, threads, secs = oracle_tokens_per_s(wl, host0, xa, budget_s=args.cpu_budget)
+        tps, done, threads, secs = oracle_tokens_per_s(wl, host0, xa, budget_s=cpu_budget, max_s=2.5 * cpu_budget)
         model, ncpu = cpu_info()
         cpu_base = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                    "sample": f"{done} independent T={wl.T} tokens of layer 0 in {secs:.1f} s "
-                              f"(batches of {threads}), {model}, {ncpu} host cores"}
+                    "sample": f"{done} independent tokens of layer 0 in {secs:.1f} s (batches of "
+                              f"{threads * min(max(1, wl.T), 4)}), {model}, {ncpu} host cores"}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
-            "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
-            "config": workload_config(wl, args),
-            "layer_hbm_gbs": layer_gbs,
-            "timed_loops_ms": loops, "timed_loop": timing,
-            "near_ties": {"tokens": near, "of": R * wl.T, "gap": NEAR_TIE,
-                          "note": "tokens of the rotating inputs whose fp64 top-(k+1) logits have an adjacent gap "
-                                  "below the threshold; their selection may follow fp32 rounding"},
-            "separate_path_ms": {"route_and_bucket": rb_ms, "expert_ffn": ffn_ms_mean},
-            "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
-            "gpu_launches": launches, "gpu_launches_source": launches_src, "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    return 0
+    del g_step, g_rb, g_ffn, g_all, layers, xs, outs, wss
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
+        "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
+        "config": workload_config(wl, args, R),
+        "layer_hbm_gbs": layer_gbs,
+        "timed_loops_ms": loops, "timed_loop": timing,
+        "near_ties": {"tokens": near, "of": R * wl.T, "gap": NEAR_TIE,
+                      "note": "tokens of the rotating inputs whose fp64 top-(k+1) logits have an adjacent gap "
+                              "below the threshold; their selection may follow fp32 rounding"},
+        "separate_path_ms": {"route_and_bucket": rb_ms, "expert_ffn": ffn_ms_mean},
+        "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+        "gpu_launches": launches, "gpu_launches_source": launches_src, "clocks": clocks,
+    }
 
 
-def run_stack(args, ws, rank, local):
+class StackWeights:
+    """The 48 resident layers of the stack workloads (they share weights and
+    routers: the same seeds), generated once."""
+
+    def __init__(self, wl, dev, keep_host0: bool):
+        self.layers, self.host0 = [], None
+        for l in range(wl.layers):
+            w = synth.make_layer(wl, l, dev)
+            if l == 0 and keep_host0:
+                self.host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
+            self.layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"],
+                                                         w["down"], w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
+            del w
+        torch.cuda.synchronize()
+
+
+def measure_stack(wl, args, ws, rank, dev, sampler, sw: StackWeights, steps: int, warmup: int, cpu_budget: float):
     """The 48-layer stack: every layer resident, one CUDA graph per step running
     x_{l+1} = x_l + MoE_l(x_l) through all layers (residual chaining through two
     ping-pong buffers).  tokens/s = T / t_stack."""
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    wl = synth.WORKLOADS[args.workload]
     act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
     tc_path = act == binding.MOE_ACT_BF16 and wl.T * wl.k >= 128
-    binding.load()
     L = wl.layers
-    layers, host0 = [], None
-    for l in range(L):
-        w = synth.make_layer(wl, l, dev)
-        if l == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
-            host0 = {k: (None if v is None else v.cpu().numpy()) for k, v in w.items()}
-        layers.append(binding.Layer.from_blocks(wl.E, wl.k, wl.d_model, wl.d_ff, w["gate"], w["up"], w["down"],
-                                                w["Wr"], w["bias"], wfmt=wfmt_of(wl)))
-        del w
+    layers = sw.layers
     x0 = synth.make_x(wl, dev, step=0)
     bufs = [torch.empty_like(x0), torch.empty_like(x0)]
     wsb = binding.workspace(wl.T, layers[0], act, 0, dev)
@@ -696,10 +657,8 @@ def run_stack(args, ws, rank, local):
     step_bytes = sum(n * expert_bytes(wl) + 2 * xbytes + wl.E * wl.d_model * 4 for n in n_active)
     kn = graph_kernel_nodes(g)
 
-    sampler = ClockSampler(local)
-    sampler.start()
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
         t_soak = time.time()
@@ -711,18 +670,17 @@ def run_stack(args, ws, rank, local):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
         t_clk1 = time.time()
     ms_local = e0.elapsed_time(e1)
-    sampler.stop()
     clocks = sampler.summary(t_clk0 - 0.5, t_clk1 + 0.05)
     ms = max_over_ranks(ms_local, ws, dev)
-    tokens = args.steps * wl.T * ws
-    value = job_rate(args.steps, wl.T, ws, ms)
+    tokens = steps * wl.T * ws
+    value = job_rate(steps, wl.T, ws, ms)
 
     # dominant kernel: the expert FFN of each layer, timed alone (routing first, outside the events)
     P = wl.T * wl.k
@@ -737,7 +695,7 @@ def run_stack(args, ws, rank, local):
     st = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
     ffn_ms, ffn_alg = [], []
     with torch.cuda.stream(stream):
-        for rep in range(3):
+        for rep in range(2):
             for l in range(L):
                 binding._check("moe_route", Lb.moe_route(binding._ptr(x0), wl.T, layers[l].ref(), binding._ptr(idx),
                                                          binding._ptr(wts), binding.ctypes.c_void_p(st())))
@@ -757,17 +715,17 @@ def run_stack(args, ws, rank, local):
     ffn_ms_mean = float(np.mean(ffn_ms))
     alg = float(np.mean(ffn_alg))
     achieved = alg / (ffn_ms_mean / 1e3) / 1e9
-    roofline = {"kernel": ("moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)" if tc_path
-                           else f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"),
+    roofline = {"kernel": expert_path_name(wl, tc_path),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": alg, "launch_ms": ffn_ms_mean, "traffic": None,
-                "timed_over": f"{len(ffn_ms)} launches, every layer of the stack"}
+                "timed_over": f"{len(ffn_ms)} launches, every layer of the stack (CUDA events on the launch stream)"}
     if tc_path:
         flops = 2.0 * wl.T * wl.k * 3 * wl.d_model * wl.d_ff
         tf = flops / (ffn_ms_mean / 1e3) / 1e12
-        roofline["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                              "frac": tf / peaks["bf16_tflops"], "flops_per_launch": flops}
+        roofline["tensor"] = {"achieved": tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                              "frac": tf / peaks["bf16_tflops_sustained"], "flops_per_launch": flops,
+                              "peak_note": "sustained bf16 figure (kernel timed inside a long step)"}
 
     # end to end: pinned x in, the stack, the final hidden state out
     xh = x0.cpu().pin_memory()
@@ -777,7 +735,7 @@ def run_stack(args, ws, rank, local):
         barrier(ws)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             x0.copy_(xh, non_blocking=True)
             g.replay()
             oh.copy_(bufs[L % 2], non_blocking=True)
@@ -787,34 +745,86 @@ def run_stack(args, ws, rank, local):
     e2e_ms = max_over_ranks(a.elapsed_time(b), ws, dev)
 
     cpu_base = None
-    if host0 is not None:
+    if sw.host0 is not None and cpu_budget > 0:
         xa = synth.make_x(wl, "cpu", step=1000, T=256).double().numpy()
-        tps, done, threads, secs = oracle_tokens_per_s(wl, host0, xa, budget_s=args.cpu_budget)
+        tps, done, threads, secs = oracle_tokens_per_s(wl, sw.host0, xa, budget_s=cpu_budget,
+                                                       max_s=2.5 * cpu_budget)
         model, ncpu = cpu_info()
         cpu_base = {"value": tps / L, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                     "sample": f"layer 0 of the stack timed on {done} independent tokens in {secs:.1f} s; "
                               f"stack rate = layer rate / {L} (extrapolated), {model}, {ncpu} host cores"}
+    del g
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
+        "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
+        "config": {"workload": f"{wl.name}: {L}-layer MoE stack with residual, T={wl.T}, d_model={wl.d_model}, "
+                               f"d_ff={wl.d_ff}, E={wl.E}, top-{wl.k}, Zipf router bias, "
+                               f"{'bf16' if tc_path else 'f32'} expert inputs",
+                   "tokens_per_step": wl.T, "layers": L,
+                   "l2": f"inputs larger than L2: {L} resident layers x {wl.E} experts x {expert_bytes(wl)} B",
+                   "parallelism": f"replicas x{ws}", "graph": f"one CUDA graph per step ({L} layers)"},
+        "stack_hbm_gbs": step_bytes / (ms_local / steps / 1e3) / 1e9,
+        "roofline": roofline, "cpu_baseline": cpu_base,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
+                "d2h_bytes_per_step": xbytes,
+                "method": "fixed protocol: x copied in from pinned host memory, the stack's step graph, the final "
+                          "hidden state copied back; serial on one stream"},
+        "gpu_launches": None if kn is None else kn * steps,
+        "gpu_launches_source": "kernel nodes of the captured step graph" if kn is not None
+        else "graph introspection unavailable",
+        "clocks": clocks,
+    }
+
+
+# The default run: the headline workload (decode T = 1), then every other
+# workload of the metric as a sub-record of the same line.
+SUITE_LAYERS = ["decode_t64_zipf", "prefill_t768", "prefill_t1024", "prefill_t2048_mb1024", "prefill_t2048"]
+SUITE_STACKS = ["stack48_t1", "stack48_t64", "stack48_t1024"]
+
+
+def run_ours(args, ws, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_start = time.time()
+    try:
+        name = args.workload or "decode_t1"
+        wl = synth.WORKLOADS[name]
+        keep_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+        if wl.layers > 1:
+            sw = StackWeights(wl, dev, keep_cpu)
+            line = measure_stack(wl, args, ws, rank, dev, sampler, sw, args.steps, args.warmup,
+                                 args.cpu_budget if keep_cpu else 0.0)
+            del sw
+        else:
+            line = measure_layer(wl, args, ws, rank, dev, sampler, args.rot, args.steps, args.warmup,
+                                 args.cpu_budget if keep_cpu else 0.0, e2e_variants=True)
+        if args.workload is None and not args.headline_only:
+            subs = {}
+            sub_cpu = args.sub_cpu_budget if keep_cpu else 0.0
+            for n in SUITE_LAYERS:
+                torch.cuda.empty_cache()
+                subs[n] = measure_layer(synth.WORKLOADS[n], args, ws, rank, dev, sampler, args.sub_rot,
+                                        args.steps, args.warmup, sub_cpu)
+            torch.cuda.empty_cache()
+            sw = StackWeights(synth.WORKLOADS[SUITE_STACKS[0]], dev, keep_cpu)
+            for n in SUITE_STACKS:
+                subs[n] = measure_stack(synth.WORKLOADS[n], args, ws, rank, dev, sampler, sw,
+                                        max(3, args.steps // 4), args.warmup, sub_cpu)
+            del sw
+            torch.cuda.empty_cache()
+            line["workloads"] = subs
+            line["workloads_note"] = ("every workload of the metric, measured in this run with the same K / W "
+                                      f"(the stacks with K/4 steps); value and ms_per_step above are "
+                                      f"{name}'s")
+        line["bench_wall_s"] = time.time() - t_start
+    finally:
+        sampler.stop()
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if tc_path else "f32",
-            "data": f"synthetic (seeded, qwen3_moe geometry, random-init {fmt_name(wl)})",
-            "config": {"workload": f"{wl.name}: {L}-layer MoE stack with residual, T={wl.T}, d_model={wl.d_model}, "
-                                   f"d_ff={wl.d_ff}, E={wl.E}, top-{wl.k}, Zipf router bias, "
-                                   f"{'bf16' if tc_path else 'f32'} expert inputs",
-                       "tokens_per_step": wl.T, "layers": L,
-                       "l2": f"inputs larger than L2: {L} resident layers x {wl.E} experts x {expert_bytes(wl)} B",
-                       "parallelism": f"replicas x{ws}", "graph": f"one CUDA graph per step ({L} layers)"},
-            "stack_hbm_gbs": step_bytes / (ms_local / args.steps / 1e3) / 1e9,
-            "roofline": roofline, "cpu_baseline": cpu_base,
-            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
-                    "d2h_bytes_per_step": xbytes},
-            "gpu_launches": None if kn is None else kn * args.steps,
-            "gpu_launches_source": "kernel nodes of the captured step graph" if kn is not None
-            else "graph introspection unavailable",
-            "clocks": clocks,
-        }
         print(json.dumps(line), flush=True)
     return 0
 
@@ -1029,7 +1039,7 @@ def run_ab_reuse(args, ws, rank, local):
     interval lies wholly below parity (the pages' predeclared bar)."""
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[args.workload or "prefill_t1024"]
     act = binding.MOE_ACT_BF16 if wl.act == "bf16" else binding.MOE_ACT_F32
     binding.load()
     R = args.rot
@@ -1113,41 +1123,6 @@ def run_ab_reuse(args, ws, rank, local):
     return 0
 
 
-def run_read_sweep(args, local):
-    """Context for the roofline fractions: how long a one-shot, cold,
-    read-only pass over N bytes of HBM takes with a library reduction
-    (torch.sum), for N from one decode layer's bytes up to GBs.  Prints one
-    JSON line; not a throughput line of this library."""
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # larger than L2: evicts between passes
-    rows = []
-    for mb in (8, 21, 27, 41, 100, 270, 1000, 4000):
-        n = mb * (1 << 20) // 4
-        nb = 4 if mb <= 1000 else 1
-        bufs = [torch.randn(n, device=dev) for _ in range(nb)]
-        for b in bufs:
-            b.sum()
-        ts = []
-        for rep in range(21):
-            b = bufs[rep % nb]
-            flush.fill_(rep & 255)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            b.sum()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        t = sorted(ts)[len(ts) // 2]
-        rows.append({"mib": mb, "us": t * 1e3, "gb_s": mb * 1.048576e6 / (t / 1e3) / 1e9})
-        del bufs
-        torch.cuda.empty_cache()
-    print(json.dumps({"read_sweep": rows, "kernel": "torch.sum over fp32, cold (L2 flushed), median of 21",
-                      "peak_hbm_gbs": load_peaks()["hbm_gbs"]}), flush=True)
-    return 0
-
-
 def sources_sha1(paths) -> str:
     """sha1 over the concatenated bytes of the given repo files (in order)."""
     import hashlib
@@ -1186,7 +1161,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(synth.WORKLOADS),
+                    help="one workload only (default: decode T=1 with every workload of the metric as sub-records)")
     ap.add_argument("--rot", type=int, default=16, help="seeded layers the steps rotate over")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -1195,8 +1171,9 @@ def main():
     ap.add_argument("--ab-reuse-order", action="store_true",
                     help="paired A/B of the reuse-ordering traversal instead of the throughput line")
     ap.add_argument("--pairs", type=int, default=16)
-    ap.add_argument("--read-sweep", action="store_true",
-                    help="time one-shot cold HBM reads of 8 MiB .. 4 GiB with a library reduction (context)")
+    ap.add_argument("--headline-only", action="store_true", help="only the headline workload (no sub-records)")
+    ap.add_argument("--sub-rot", type=int, default=4, help="seeded layers the sub-record workloads rotate over")
+    ap.add_argument("--sub-cpu-budget", type=float, default=4.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1204,14 +1181,10 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, ws, rank)
-        if args.read_sweep:
-            return run_read_sweep(args, local)
         if args.ab_reuse_order:
             return run_ab_reuse(args, ws, rank, local)
-        if synth.WORKLOADS[args.workload].arena_slots > 0:
+        if args.workload and synth.WORKLOADS[args.workload].arena_slots > 0:
             return run_arena(args, ws, rank, local)
-        if synth.WORKLOADS[args.workload].layers > 1:
-            return run_stack(args, ws, rank, local)
         return run_ours(args, ws, rank, local)
     finally:
         if ws > 1:

@@ -1,6 +1,7 @@
 // C ABI of libmoe_gb300: argument checks, workspace carving and the launch
 // sequence of the routed MoE layer.  Every entry point only enqueues work on
 // the caller's stream; nothing here synchronises or reads back.
+#include <atomic>
 #include <limits.h>
 
 #include "common.cuh"
@@ -79,24 +80,28 @@ bool valid_experts(const moe_layer_w* w) {
 }
 
 // sm_103 (GB300) only: the library is built for sm_103a.
+// The per-device answer is cached lock-free (threads racing on the first
+// call store the same value).
 int check_device() {
-    static int cached[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+    static std::atomic<int> cached[64];  // 0 unknown, 1 ok, 2 unsupported (zero-initialised)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-    if (cached[dev] == 0) {
+    int c = cached[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
-        cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+        c = (major == 10 && minor == 3) ? 1 : 2;
+        cached[dev].store(c, std::memory_order_relaxed);
     }
-    return cached[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+    return c == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
 // Expert path: bf16 activations -> tcgen05 kernels when the batch fills at

@@ -24,6 +24,8 @@
 //       h[p][r] = silu(Wg[e][r] . x_p) * (Wu[e][r] . x_p)
 //   down item:    32 output rows o, pairs p of one bucket chunk:
 //       out[tok(p)][o] += w(p) * (Wd[e][o] . h[p])      (or ypairs[p][o])
+#include <atomic>
+
 #include "common.cuh"
 #include "pipeline.cuh"
 #include "stream_common.cuh"
@@ -450,16 +452,18 @@ __global__ void __launch_bounds__(NW * 32, 1) down_rows_kernel(
 }
 
 int rows_num_sms() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised; racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
+    int c = cached[dev].load(std::memory_order_relaxed);
+    if (!c) {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 148;
+        c = n > 0 ? n : 148;
+        cached[dev].store(c, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return c;
 }
 
 template <typename K, typename... Args>

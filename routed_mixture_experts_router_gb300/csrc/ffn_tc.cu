@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded: past the deadline the CTA flags
 // MOE_STATUS_TIMEOUT in the status word and stops; all copies and MMAs it
 // started are drained before TMEM is freed.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -439,7 +440,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = ew * 32 + lane;   // weight row within the unit
         const int et = ew * 32 + lane;    // pair slot staged by this thread
         uint32_t uc = 0;
-        for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+            // the four epilogue warps leave together or not at all: they meet
+            // at named barrier 2 below, so one warp leaving alone would strand
+            // the others there
+            if (!named_bar_and(2, 128, !s_abort)) break;
             const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
             if (EPI == 1) {
                 int tok = -1;
@@ -457,7 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 named_bar(2, 128);
             }
             const int buf = uc & 1;
-            if (!tc_wait(acc_full + buf, (uc >> 1) & 1, p.status, &s_abort)) break;
+            const bool landed = tc_wait(acc_full + buf, (uc >> 1) & 1, p.status, &s_abort);
+            if (!named_bar_and(2, 128, landed)) break;  // a timeout in any epilogue warp ends all four
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + buf * NMAT * kBN;
             for (int c0 = 0; c0 < U.N; c0 += 16) {
@@ -527,18 +533,22 @@ __global__ void gather_bf16_kernel(const float* __restrict__ x, int T, int dm, c
 }
 
 // ------------------------------------------------------------------ host side
+// Looked up once (racing first calls store the same pointer).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f0 = fn.load(std::memory_order_acquire);
+    if (!f0) {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+            q == cudaDriverEntryPointSuccess) {
+            f0 = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+            fn.store(f0, std::memory_order_release);
+        }
         cudaGetLastError();
     }
-    return fn;
+    return f0;
 }
 
 // 2-D K-major map: inner dimension K (elements), outer `rows`, box {bx, by}, 128-byte swizzle.

@@ -12,6 +12,7 @@
 // cluster barrier the leader's threads rank the logits (top-k by rank, one
 // thread per (token, expert) candidate).  No global scratch, no atomics, no
 // inter-CTA spin: deterministic.
+#include <atomic>
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -161,12 +162,12 @@ cudaError_t launch_route_tt(const float* x, int T, const moe_layer_w& w, int32_t
 // Largest cluster size (16, else 8) that the device can co-schedule for this
 // kernel shape; probed once per process and device.
 int route_cluster_size(int E, size_t smem) {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised; racing first calls store the same value
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
     int want = E >= 128 ? 16 : 8;
     if (want == 16) {
-        if (cached[dev] == 0) {
+        if (cached[dev].load(std::memory_order_relaxed) == 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(16, 1, 1);
             cfg.blockDim = dim3(kRouteThreads, 1, 1);
@@ -183,10 +184,10 @@ int route_cluster_size(int E, size_t smem) {
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             cudaError_t err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            cached[dev] = (err == cudaSuccess && n > 0) ? 16 : 8;
+            cached[dev].store((err == cudaSuccess && n > 0) ? 16 : 8, std::memory_order_relaxed);
             cudaGetLastError();
         }
-        want = cached[dev];
+        want = cached[dev].load(std::memory_order_relaxed);
     }
     return want;
 }

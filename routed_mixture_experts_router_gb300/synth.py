@@ -58,6 +58,7 @@ class Workload:
     residual: bool = False
     wfmt: str = "q8"  # expert weight blocks: "q8" (Q8_0, 34 B) or "q4" (Q4_0, 18 B)
     arena_slots: int = 0  # > 0: experts served from an arena of this many HBM slots
+    microbatch: int = 0   # > 0: the T tokens run as T / microbatch layer calls of this many tokens
 
 
 WORKLOADS = {
@@ -71,6 +72,9 @@ WORKLOADS = {
     "prefill_t1024": Workload("prefill_t1024", 4, 1024, 2048, 768, 128, 8, act="bf16"),
     "prefill_t768": Workload("prefill_t768", 4, 768, 2048, 768, 128, 8, act="bf16"),
     "prefill_t2048": Workload("prefill_t2048", 4, 2048, 2048, 768, 128, 8, act="bf16"),
+    # the same 2048 tokens as two 1024-token microbatches (two layer calls)
+    "prefill_t2048_mb1024": Workload("prefill_t2048_mb1024", 4, 2048, 2048, 768, 128, 8, act="bf16",
+                                     microbatch=1024),
     # 48-layer stack, residual between layers, Zipf routing; T in {1, 64, 1024}
     "stack48_t1": Workload("stack48_t1", 5, 1, 2048, 768, 128, 8, zipf=True, layers=48, residual=True),
     "stack48_t64": Workload("stack48_t64", 5, 64, 2048, 768, 128, 8, zipf=True, layers=48, residual=True),
