@@ -500,14 +500,16 @@ def measure_layer(wl, args, ws, rank, dev, sampler, rot: int, steps: int, warmup
         fused_ms = ms_local / steps
         step_alg0 = float(np.mean([step_bytes[i % R] for i in range(steps)]))
         fa = step_alg0 / (fused_ms / 1e3) / 1e9
-        roofline = {"kernel": f"decode_fused_kernel (whole layer: router, top-k, bucketing, {fmt_name(wl)} "
+        kname = "decode_fused_kernel" if wl.wfmt == "q4" else "decode_split_kernel"
+        roofline = {"kernel": f"{kname} (whole layer: router, top-k, bucketing, {fmt_name(wl)} "
                               "gate/up + down, combine; one cooperative launch)",
                     "bound": "hbm", "achieved": fa, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": fa / peaks["hbm_gbs"], "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": step_alg0, "launch_ms": fused_ms,
-                    "launch_ms_note": "per step of the timed loop (CUDA events on the launch stream): the kernel "
-                                      "plus the memset of its synchronisation words (the step graph's two nodes)",
-                    "traffic": load_traffic(f"decode_fused_kernel {wl.name}"),
+                    "launch_ms_note": "per step of the timed loop (CUDA events on the launch stream): the step "
+                                      "graph's kernel node" + (" and the memset of its barrier words"
+                                                               if kname == "decode_fused_kernel" else ""),
+                    "traffic": load_traffic(f"{kname} {wl.name}"),
                     "expert_ffn_three_kernel_path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
                                                      "launch_ms": ffn_ms_mean}}
     if tc_path:

@@ -38,7 +38,8 @@ WsLayout ws_layout(int T, const moe_layer_w& w, int act, int flags) {
     if (act == MOE_ACT_BF16) o = align_up(o + P * (size_t)w.d_model * sizeof(uint16_t));
     L.ypairs = o;
     if (flags & MOE_FLAG_DETERMINISTIC) o = align_up(o + P * (size_t)w.d_model * sizeof(float));
-    L.lg = o;     o = align_up(o + (size_t)T * w.E * sizeof(float));         // router logits (fused decode)
+    L.lg = o;                                                               // router logits (decode kernels)
+    o = align_up(o + (T >= 1 && T <= 2 ? decode_split_words(T, w.E) : (size_t)T * w.E) * sizeof(unsigned long long));
     L.sync = o;   o = align_up(o + 2 * sizeof(unsigned int));               // grid-barrier words (fused decode)
     L.smap = o;   o = align_up(o + (size_t)w.E * sizeof(int32_t));           // expert -> arena slot map
     L.total = o;
@@ -60,7 +61,8 @@ bool valid_geometry(const moe_layer_w* w) {
 bool ffn_supported(const moe_layer_w* w, int T, int act) {
     if (w->wfmt == MOE_WFMT_Q4_0) return ffn_rows_supported(*w, T > 0 ? T : 1);
     if (!w->expert_slot) return true;
-    return (act == MOE_ACT_BF16 && ffn_tc_supported(*w, T)) || ffn_rows_supported(*w, T) || ffn_stream_supported(*w);
+    return (act == MOE_ACT_BF16 && ffn_tc_supported(*w, T)) || ffn_rows_supported(*w, T) ||
+           (ffn_stream_supported(*w) && ffn_stream_fits(*w, T > 0 ? T : 1));
 }
 
 bool valid_T(int T, const moe_layer_w* w) { return T >= 0 && T <= 65536 && (long long)T * w->k <= INT_MAX / 2; }
@@ -125,7 +127,7 @@ cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, con
                              status, reuse_order, s);
     if (ffn_rows_supported(w, T))
         return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
-    if (ffn_stream_supported(w))
+    if (ffn_stream_supported(w) && ffn_stream_fits(w, T))
         return launch_ffn_stream(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, status, s);
     if (w.expert_slot) return cudaErrorNotSupported;  // the per-expert-CTA kernels read weights in expert order
     return launch_ffn_f32(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
@@ -279,6 +281,14 @@ int moe_layer_forward(const float* x, int T, const moe_layer_w* w, int act, int 
     // cooperative launch (falls through to the separate kernels if the device
     // cannot co-schedule it).
     const bool f32_path = act == MOE_ACT_F32 || !ffn_tc_supported(*w, T);
+    if (f32_path && !(flags & MOE_FLAG_DETERMINISTIC) && decode_split_supported(*w, T)) {
+        const cudaError_t fe = launch_decode_split(x, T, *w, residual, out, idx_out, wts_out, offsets_out,
+                                                   reinterpret_cast<unsigned long long*>(base + L.lg),
+                                                   reinterpret_cast<unsigned int*>(base + L.sync), status, s);
+        if (fe == cudaSuccess) return MOE_OK;
+        if (fe != cudaErrorInvalidConfiguration && fe != cudaErrorCooperativeLaunchTooLarge) return cuda_rc(fe);
+        cudaGetLastError();
+    }
     if (f32_path && !(flags & MOE_FLAG_DETERMINISTIC) && decode_fused_supported(*w, T)) {
         const cudaError_t fe = launch_decode_fused(x, T, *w, residual, out, idx_out, wts_out, offsets_out,
                                                    reinterpret_cast<float*>(base + L.lg),

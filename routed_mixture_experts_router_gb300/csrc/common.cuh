@@ -102,6 +102,7 @@ cudaError_t launch_ffn_rows(const float* x, int T, const moe_layer_w& w, const i
                             const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                             float* out_or_ypairs, int residual, float* h, cudaStream_t s);
 bool ffn_stream_supported(const moe_layer_w& w);
+bool ffn_stream_fits(const moe_layer_w& w, int T);  // shared memory of the configuration picked for T
 cudaError_t launch_ffn_stream(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                               const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                               float* out_or_ypairs, int residual, float* h, int32_t* status, cudaStream_t s);
@@ -119,6 +120,17 @@ bool decode_fused_supported(const moe_layer_w& w, int T);
 cudaError_t launch_decode_fused(const float* x, int T, const moe_layer_w& w, int residual, float* out,
                                 int32_t* idx_out, float* wts_out, int32_t* offsets_out, float* logits, float* h,
                                 unsigned int* sync, int32_t* status, cudaStream_t s);
+
+// The whole layer for T <= 2 decode tokens in one cooperative launch with a
+// single grid-wide exchange (the router logits), the down projection split
+// along K with each CTA's gate/up features (Q8_0, fp32 path).  lgw:
+// decode_split_words(T, E) 8-byte workspace words, epoch: one 4-byte
+// workspace word (any contents; calls sharing a workspace must not overlap).
+bool decode_split_supported(const moe_layer_w& w, int T);
+cudaError_t launch_decode_split(const float* x, int T, const moe_layer_w& w, int residual, float* out,
+                                int32_t* idx_out, float* wts_out, int32_t* offsets_out, unsigned long long* lgw,
+                                unsigned int* epoch, int32_t* status, cudaStream_t s);
+size_t decode_split_words(int T, int E);
 
 cudaError_t launch_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, cudaStream_t s);
 cudaError_t launch_pack_q4(const uint8_t* blocks, long long rows, int K, uint8_t* qs, uint16_t* d, cudaStream_t s);

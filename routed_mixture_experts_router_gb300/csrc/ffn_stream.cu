@@ -342,6 +342,23 @@ cudaError_t down_dispatch(const float* h, int T, const moe_layer_w& w, const int
 
 }  // namespace
 
+// Whether both kernels' shared memory (rings + staged activations), in the
+// configuration the dispatch above picks for T tokens, fits the cap.
+bool ffn_stream_fits(const moe_layer_w& w, int T) {
+    const int dm = w.d_model, f = w.d_ff, P = T * w.k;
+    const int kg = (dm / 16 + 31) / 32, KCHg = kg <= 2 ? kg : 4;
+    const int kd = (f / 16 + 15) / 16, KCHd = kd <= 3 ? kd : 4;
+    const int tca = T <= kMultiG ? T : kMultiG;
+    const bool alltok = T <= kMultiG && P <= kMaxStagedPairs;
+    const int nwg = (T <= 2 && alltok) ? 16 : 12;
+    const size_t gu = (size_t)nwg * 3 * (2 * dm + 2 * (dm / 16)) + (size_t)tca * KCHg * 4 * 32 * 16;
+    const size_t tok_bytes = (size_t)KCHd * 4 * 16 * 16;
+    const bool allp = (size_t)P * tok_bytes <= 48 * 1024 && P <= kMaxStagedPairs;
+    const int tcp = (allp && (T <= 2 || T <= kMultiG)) ? P : kMultiG;
+    const size_t dn = (size_t)16 * 3 * (kDnRowsPerItem * f + kDnRowsPerItem * (f / 16)) + (size_t)tcp * tok_bytes;
+    return gu <= kSmemCap && dn <= kSmemCap;
+}
+
 bool ffn_stream_supported(const moe_layer_w& w) {
     // whole 16-byte pieces of weights and of each row's scales: K % 256 == 0;
     // down items are 4 whole rows; at most 4 chunks per lane.

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from routed_mixture_experts_router_gb300 import binding, synth
-from gpu_util import TOL_BF16, TOL_F32, check_routing, near_tie_mask, rel_l2_max
+from gpu_util import NEAR_TIE, TOL_BF16, TOL_F32, check_routing, rel_l2_max
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,9 @@ def _stack_chain(name, nlayers, tokens=None, tol=TOL_F32, final_tol=None):
     error against the oracle fed bf16-rounded expert inputs is printed as a
     diagnostic only.  Near-tie tokens (adjacent top-(k+1) fp64 gap < 1e-5)
     are counted; where the GPU's selection is a valid top-k that differs from
-    the oracle's, both oracle runs take the GPU's selection for that layer.
+    the oracle's, both oracle runs take the GPU's selection for that layer
+    (in the free-running chain: a valid top-k within twice the logit drift
+    between the two chains' hidden states).
     Only the sampled `tokens` are computed on the CPU (tokens are
     independent, so their chain does not depend on the others)."""
     wl = synth.WORKLOADS[name]
@@ -86,8 +88,17 @@ def _stack_chain(name, nlayers, tokens=None, tol=TOL_F32, final_tol=None):
         f_out, f_idx, f_w, f_l = orc.moe_layer(x_free, *args, residual=True)
         diff = np.nonzero((f_idx != gidx).any(axis=1))[0]
         if diff.size:
-            # only near-ties of the oracle's own chain may route differently
-            assert near_tie_mask(f_l[diff], wl.k).all(), f"layer {l}: free-running routing differs off a near-tie"
+            # The two chains' hidden states differ by the accumulated rounding
+            # of the earlier layers, which moves each logit by at most
+            # dl = max |l_oracle_chain - l_on_gpu_state|; a selection can flip
+            # only where the oracle chain's own logits leave the GPU's
+            # selection within 2 dl (+ the near-tie gap) of a valid top-k.
+            for t in diff:
+                dl = float(np.abs(f_l[t] - o_l[t]).max())
+                sel_l = f_l[t, gidx[t]]
+                rest = np.delete(f_l[t], gidx[t])
+                assert sel_l.min() >= rest.max() - (2.0 * dl + NEAR_TIE), \
+                    f"layer {l}: token {sel[t]} free-running routing differs beyond the chains' logit drift {dl:.2e}"
             flips += int(diff.size)
             f_out = orc.moe_layer(x_free, *args, residual=True, forced_idx=gidx)[0]
         x_free = f_out
@@ -112,10 +123,18 @@ def test_stack48_t64_all_layers():
     _stack_chain("stack48_t64", 48)
 
 
+# The bf16 tolerance is per layer (teacher-forced, above).  Free-running, the
+# hidden state carries 48 layers of bf16 operand rounding (measured 1.4e-2 at
+# the final layer against the oracle's own chain, with every layer inside
+# 4e-3); that figure is printed, and bounded only loosely (5e-2) as a check
+# that nothing beyond compounded rounding separates the two chains.
+BF16_STACK_FINAL_BOUND = 5e-2
+
+
 def test_stack48_t1024_bf16_all_layers_sampled():
     tokens = np.sort(np.random.default_rng(7).choice(1024, size=16, replace=False))
     tokens[0], tokens[-1] = 0, 1023
-    _stack_chain("stack48_t1024", 48, tokens=tokens, tol=TOL_BF16)
+    _stack_chain("stack48_t1024", 48, tokens=tokens, tol=TOL_BF16, final_tol=BF16_STACK_FINAL_BOUND)
 
 
 @pytest.mark.parametrize("flags", [binding.MOE_FLAG_DETERMINISTIC, 0], ids=["det", "atomic"])
