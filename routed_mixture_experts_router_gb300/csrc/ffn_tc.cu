@@ -21,11 +21,15 @@
 //   warp 2       TMA producer: bf16 token tiles (N x 64 K) into the operand
 //                ring (separate, so the weight stream never waits on it)
 //   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, M=128,
-//                K=16 per instruction, into a double-buffered TMEM accumulator
+//                K=16 per instruction, A from TMEM, B from shared memory,
+//                into TMEM accumulators (double-buffered for the down
+//                projection, single for gate/up, whose two matrices fill
+//                the columns the A stages leave)
 //   warps 4-11   dequantisation: thread = (row, half of each 64-K operand
 //                stage); int8 -> fp32 exactly, times the block's fp16 scale,
-//                -> bf16 (RNE), written in the 128-byte-swizzled K-major
-//                layout the MMA reads
+//                -> bf16 (RNE), stored straight into TMEM (lane = weight row,
+//                its warp's lane quadrant) as the MMA's A operand: no
+//                shared-memory round trip for the dequantised weights
 //   warps 12-15  epilogue: tcgen05.ld of the accumulator (TMEM lane = row),
 //                SwiGLU -> bf16 h, or the weighted combine into out
 // Every mbarrier wait is bounded: past the deadline the CTA flags
@@ -56,10 +60,15 @@ constexpr int kBRows = 32;    // token rows per TMA box
 // operand (bf16) ring keeps only the depth the dequant -> MMA hand-off needs.
 template <int NMAT>
 struct TcRing {
-    static constexpr int RS = NMAT == 2 ? 3 : 6;  // raw stages (NMAT x 16 KB each)
-    static constexpr int AS = NMAT == 2 ? 2 : 3;  // operand stages (NMAT A tiles + one B tile)
+    static constexpr int RS = NMAT == 2 ? 4 : 6;  // raw stages (NMAT x (16 KB + 2 KB scales), shared memory)
+    static constexpr int AS = 4;                  // operand stages: NMAT bf16 A tiles in TMEM + one B tile
+    static constexpr int NBUF = NMAT == 2 ? 1 : 2;  // accumulator buffers (TMEM)
+    static constexpr uint32_t ACC_COLS = NMAT * kBN * NBUF;
+    static constexpr uint32_t A_COLS = kBK / 2;   // one bf16 A tile (128 rows x 64 K): 32 columns
+    static_assert(ACC_COLS + AS * NMAT * A_COLS <= 512, "TMEM budget");
 };
 constexpr int kTile = 16384;  // one 128 x 128-byte tile
+constexpr int kScTile = 2048;  // scales of one raw stage: 128 rows x 8 fp16 (a 16-byte aligned window)
 constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12;
 
 struct TcParams {
@@ -231,13 +240,16 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int32_t*
 template <int NMAT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                  const __grid_constant__ CUtensorMap tm_b, TcParams p) {
+                  const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_s0,
+                  const __grid_constant__ CUtensorMap tm_s1, TcParams p) {
     constexpr int kRS = TcRing<NMAT>::RS;
     constexpr int AS = TcRing<NMAT>::AS;
-    constexpr uint32_t kTmemCols = NMAT * kBN * 2;
+    constexpr int NBUF = TcRing<NMAT>::NBUF;
+    constexpr uint32_t kTmemCols = 512;  // accumulators, then the A operand stages
+    constexpr uint32_t kAcol0 = TcRing<NMAT>::ACC_COLS;
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[kRS], raw_empty[kRS], b_full[AS], a_full[AS], ab_empty[AS];
-    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain_bar;
+    __shared__ __align__(8) uint64_t acc_full[NBUF], acc_empty[NBUF], drain_bar;
     __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
     __shared__ int s_cb[MOE_MAX_EXPERTS + 1], s_n;
     __shared__ uint32_t s_tmem;
@@ -248,8 +260,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char* raw = smem;                                   // [kRS][NMAT][kTile]
-    unsigned char* As = raw + kRS * NMAT * kTile;                // [AS][NMAT][kTile]
-    unsigned char* Bs = As + AS * NMAT * kTile;                  // [AS][kTile]
+    unsigned char* Bs = raw + kRS * NMAT * kTile;                // [AS][kTile]
+    unsigned char* Ss = Bs + AS * kTile;                         // [kRS][NMAT][128 rows][8 scales]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(a_full + s, kDqWarps);
             mbar_init(ab_empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             mbar_init(acc_full + b, 1);
             mbar_init(acc_empty + b, 4);
         }
@@ -273,7 +285,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_a0);
-        if (NMAT == 2) prefetch_tmap(&tm_a1);
+        prefetch_tmap(&tm_s0);
+        if (NMAT == 2) {
+            prefetch_tmap(&tm_a1);
+            prefetch_tmap(&tm_s1);
+        }
         prefetch_tmap(&tm_b);
     }
     pdl_wait();  // bucketing and the previous stage's activations are complete
@@ -300,10 +316,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int kr = 0; kr < kr_n; ++kr) {
                     const int rs = rc % kRS;
                     if (!tc_wait(raw_empty + rs, ((rc / kRS) & 1) ^ 1, p.status, &s_abort)) break;
-                    mbar_arrive_expect_tx(raw_full + rs, NMAT * kTile);
+                    mbar_arrive_expect_tx(raw_full + rs, NMAT * (kTile + kScTile));
+                    // the stage's 128 K of int8 weights, and eight fp16 scales per
+                    // row (16-byte aligned window) that hold its four blocks
                     tma_load_2d_hint(raw + (rs * NMAT + 0) * kTile, &tm_a0, kr * kBKR, wrow, raw_full + rs, pol);
-                    if (NMAT == 2)
+                    tma_load_2d(Ss + (rs * NMAT + 0) * kScTile, &tm_s0, (4 * kr) & ~7, wrow, raw_full + rs);
+                    if (NMAT == 2) {
                         tma_load_2d_hint(raw + (rs * NMAT + 1) * kTile, &tm_a1, kr * kBKR, wrow, raw_full + rs, pol);
+                        tma_load_2d(Ss + (rs * NMAT + 1) * kScTile, &tm_s1, (4 * kr) & ~7, wrow, raw_full + rs);
+                    }
                     ++rc;
                 }
             }
@@ -337,8 +358,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t ac = 0, uc = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x, ++uc) {
                 const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
-                const int buf = uc & 1;
-                if (!tc_wait(acc_empty + buf, ((uc >> 1) & 1) ^ 1, p.status, &s_abort)) break;
+                const int buf = uc % NBUF;
+                if (!tc_wait(acc_empty + buf, ((uc / NBUF) & 1) ^ 1, p.status, &s_abort)) break;
                 tc_fence_after();
                 const uint32_t idesc = umma_idesc_bf16(kBM, U.N);
                 const uint32_t dcol = tmem + buf * NMAT * kBN;
@@ -350,10 +371,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint64_t bdesc = umma_desc_sw128(Bs + s * kTile);
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
-                        const uint64_t adesc = umma_desc_sw128(As + (s * NMAT + mat) * kTile);
+                        // A: 128 TMEM lanes (weight rows) x 64 bf16 (32 columns); 16 K = 8 columns per MMA
+                        const uint32_t acol = tmem + kAcol0 + (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
-                            umma_bf16(dcol + mat * kBN, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
+                        for (int kk = 0; kk < kBK / 16; ++kk)  // B: 16 bf16 = 32 bytes = 2 descriptor units
+                            umma_bf16_ta(dcol + mat * kBN, acol + 8 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
                     }
                     umma_commit(ab_empty + s);
                     ++ac;
@@ -369,68 +391,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------------------------------------------------------- dequantisation
         const int tq = (warp - kDqWarp0) * 32 + lane;
         const int r = tq & (kBM - 1), hf = tq >> 7;  // row, half (one Q8_0 block) of each 64-K operand stage
-        const int nbk = p.K / 32;                    // scale blocks per row
         uint32_t rc = 0, ac = 0;
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
-            const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
-            const size_t srow = (size_t)(U.e * p.rows + U.m0 + r) * nbk;
-            // this thread's scales for raw stage kr: blocks 4kr + 2j + hf, j = 0, 1.
-            // Four register sets on rotating stages, each refilled (for stage
-            // kr + 4) right after its use: no move ever waits on a load, and
-            // every scale load has three raw stages (several microseconds) to
-            // land.  Raw fp16 bits, converted at the use.
-            unsigned short sa[NMAT][2], sb[NMAT][2], sc2[NMAT][2], sd[NMAT][2];
-            auto fetch = [&](int kr, unsigned short (&sc)[NMAT][2]) {
-#pragma unroll
-                for (int mat = 0; mat < NMAT; ++mat) {
-                    const unsigned short* dp = reinterpret_cast<const unsigned short*>(mat == 0 ? p.d0 : p.d1);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) sc[mat][j] = kr < kr_n ? __ldg(dp + srow + 4 * kr + 2 * j + hf) : 0;
-                }
-            };
-            auto stage = [&](int kr, unsigned short (&sc)[NMAT][2]) -> bool {
+            bool ok = true;
+            for (int kr = 0; kr < kr_n && ok; ++kr) {
                 const int rs = rc % kRS;
-                if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) return false;
-                for (int j = 0; j < 2; ++j) {
+                if (!tc_wait(raw_full + rs, (rc / kRS) & 1, p.status, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                for (int j = 0; j < 2 && ok; ++j) {
                     const int s = ac % AS;
-                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) return false;
+                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
                         const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
-                        unsigned char* at = As + (s * NMAT + mat) * kTile;
-                        const float d = __half2float(__ushort_as_half(j == 0 ? sc[mat][0] : sc[mat][1]));
+                        // this thread's block 4kr + 2j + hf, from the stage's scale window
+                        const __half* sc = reinterpret_cast<const __half*>(Ss + (rs * NMAT + mat) * kScTile);
+                        const float d = __half2float(sc[r * 8 + ((4 * kr) & 7) + 2 * j + hf]);
                         const f32x2 dd = f2_pack(d, d);
                         const f32x2 cc = f2_pack(-32896.0f * d, -32896.0f * d);
+                        uint32_t v[16];  // this thread's row: 32 bf16 (K half hf of the 64-K stage)
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + 2 * hf + i));
                             uint4 o0, o1;
                             dequant16(q, dd, cc, o0, o1);
-                            *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i)) = o0;
-                            *reinterpret_cast<uint4*>(at + sw128(r, 4 * hf + 2 * i + 1)) = o1;
+                            v[8 * i + 0] = o0.x, v[8 * i + 1] = o0.y, v[8 * i + 2] = o0.z, v[8 * i + 3] = o0.w;
+                            v[8 * i + 4] = o1.x, v[8 * i + 5] = o1.y, v[8 * i + 6] = o1.z, v[8 * i + 7] = o1.w;
                         }
+                        // TMEM lane = weight row (this warp's lane quadrant), 16 columns = 32 bf16
+                        tmem_st16(tmem + ((uint32_t)(r & ~31) << 16) + kAcol0 +
+                                      (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS + 16 * hf,
+                                  v);
                     }
-                    fence_proxy_async_smem();
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(a_full + s);
                     ++ac;
                 }
+                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty + rs);
                 ++rc;
-                fetch(kr + 4, sc);
-                return !s_abort;
-            };
-            fetch(0, sa);
-            fetch(1, sb);
-            fetch(2, sc2);
-            fetch(3, sd);
-            bool ok = true;
-            for (int kr = 0; kr < kr_n && ok; kr += 4) {
-                ok = stage(kr, sa);
-                if (ok && kr + 1 < kr_n) ok = stage(kr + 1, sb);
-                if (ok && kr + 2 < kr_n) ok = stage(kr + 2, sc2);
-                if (ok && kr + 3 < kr_n) ok = stage(kr + 3, sd);
+                ok = !s_abort;
             }
             if (!ok) break;
         }
@@ -461,8 +470,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 s_ep_w[et] = w;
                 named_bar(2, 128);
             }
-            const int buf = uc & 1;
-            const bool landed = tc_wait(acc_full + buf, (uc >> 1) & 1, p.status, &s_abort);
+            const int buf = uc % NBUF;
+            const bool landed = tc_wait(acc_full + buf, (uc / NBUF) & 1, p.status, &s_abort);
             if (!named_bar_and(2, 128, landed)) break;  // a timeout in any epilogue warp ends all four
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + buf * NMAT * kBN;
@@ -551,9 +560,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return f0;
 }
 
-// 2-D K-major map: inner dimension K (elements), outer `rows`, box {bx, by}, 128-byte swizzle.
+// 2-D K-major map: inner dimension K (elements), outer `rows`, box {bx, by},
+// 128-byte swizzle (or none).
 bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t K, uint64_t rows,
-               uint32_t bx, uint32_t by) {
+               uint32_t bx, uint32_t by, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {K, rows};
@@ -561,7 +571,7 @@ bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
     const cuuint32_t box[2] = {bx, by};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -573,11 +583,11 @@ int tc_num_sms() {
 }
 
 template <int NMAT, int EPI>
-cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const TcParams& p,
-                      cudaStream_t s) {
+cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& s0,
+                      const CUtensorMap& s1, const TcParams& p, cudaStream_t s) {
     constexpr int kRS = TcRing<NMAT>::RS;
     constexpr int AS = TcRing<NMAT>::AS;
-    const size_t smem = (size_t)(kRS * NMAT + AS * NMAT + AS) * kTile + 1024;
+    const size_t smem = (size_t)(kRS * NMAT + AS) * kTile + (size_t)kRS * NMAT * kScTile + 1024;
     auto kern = tc_ffn_kernel<NMAT, EPI>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -591,14 +601,16 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a0, a1, b, p);
+    return cudaLaunchKernelEx(&cfg, kern, a0, a1, b, s0, s1, p);
 }
 
 }  // namespace
 
 bool ffn_tc_supported(const moe_layer_w& w, int T) {
-    return w.wfmt == MOE_WFMT_Q8_0 && w.d_model % kBKR == 0 && w.d_ff % kBKR == 0 && w.d_model % kBM == 0 && w.d_ff % kBM == 0 &&
-           (long long)T * w.k >= kBN && encode_fn() != nullptr;
+    // K a multiple of 256: whole 128-K raw stages, and rows of scales (K / 32
+    // fp16) a multiple of 16 bytes, as a tensor map's row pitch must be
+    return w.wfmt == MOE_WFMT_Q8_0 && w.d_model % 256 == 0 && w.d_ff % 256 == 0 && w.d_model % kBM == 0 &&
+           w.d_ff % kBM == 0 && (long long)T * w.k >= kBN && encode_fn() != nullptr;
 }
 
 cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
@@ -621,11 +633,14 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
                                              fuse_combine ? out_or_ypairs : (float*)nullptr, residual);
         if (err != cudaSuccess) return err;
     }
-    CUtensorMap tg, tu, td, txb, th;
+    CUtensorMap tg, tu, td, txb, th, sg, su, sd;
     const uint64_t ns = (uint64_t)weight_slots(w);
     if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
         !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
         !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, ns * dm, kBKR, kBM) ||
+        !make_tmap(&sg, w.gate.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dm / 32, ns * f, 8, kBM, false) ||
+        !make_tmap(&su, w.up.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dm / 32, ns * f, 8, kBM, false) ||
+        !make_tmap(&sd, w.down.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, f / 32, ns * dm, 8, kBM, false) ||
         !make_tmap(&txb, xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dm, P, kBK, kBRows) ||
         !make_tmap(&th, hb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f, P, kBK, kBRows))
         return cudaErrorInvalidValue;
@@ -645,7 +660,7 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pg.status = status;
     pg.eslot = w.expert_slot;
     pg.nslots = (int)ns;
-    cudaError_t err = launch_tc<2, 0>(tg, tu, txb, pg, s);
+    cudaError_t err = launch_tc<2, 0>(tg, tu, txb, sg, su, pg, s);
     if (err != cudaSuccess) return err;
     TcParams pd = pg;
     pd.K = f;
@@ -655,8 +670,8 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pd.h = nullptr;
     pd.out = out_or_ypairs;
     pd.band = (reuse_order && (dm / kBM) % kReuseBand == 0) ? kReuseBand : 0;
-    if (fuse_combine) return launch_tc<1, 1>(td, td, th, pd, s);
-    return launch_tc<1, 2>(td, td, th, pd, s);
+    if (fuse_combine) return launch_tc<1, 1>(td, td, th, sd, sd, pd, s);
+    return launch_tc<1, 2>(td, td, th, sd, sd, pd, s);
 }
 
 }  // namespace moe

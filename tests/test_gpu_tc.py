@@ -56,8 +56,8 @@ def _wl(name, T, d, f, E, k, zipf=False):
 
 @pytest.mark.parametrize("shape", [
     ("tc_small", 64, 256, 256, 16, 8, False),
-    ("tc_zipf", 100, 512, 384, 32, 4, True),
-    ("tc_k2", 96, 256, 128, 8, 2, False),
+    ("tc_zipf", 100, 512, 768, 32, 4, True),
+    ("tc_k2", 96, 768, 256, 8, 2, False),
 ], ids=lambda s: s[0])
 def test_tc_layer_small(shape):
     _check(make_case(_wl(*shape)))
