@@ -12,7 +12,7 @@
 // from the first experiment"); activations cast for the expert contraction
 // ("including routing and quantization", same page, "Operator gains ...").
 //
-// Design (one persistent 512-thread CTA per SM).  A work unit is one expert,
+// Design (one persistent 640-thread CTA per SM).  A work unit is one expert,
 // one 128-row tile of its weight matrix (the MMA M dimension: "swap AB", so
 // the small, ragged token count is N) and up to 128 of its tokens (N, padded
 // to a multiple of 16).  Warp roles:
@@ -30,7 +30,8 @@
 //                -> bf16 (RNE), stored straight into TMEM (lane = weight row,
 //                its warp's lane quadrant) as the MMA's A operand: no
 //                shared-memory round trip for the dequantised weights
-//   warps 12-15  epilogue: tcgen05.ld of the accumulator (TMEM lane = row),
+//   warps 12-19  epilogue (two per TMEM lane quadrant, alternate 16-token
+//                column chunks): tcgen05.ld of the accumulator (lane = row),
 //                SwiGLU -> bf16 h, or the weighted combine into out
 // Every mbarrier wait is bounded: past the deadline the CTA flags
 // MOE_STATUS_TIMEOUT in the status word and stops; all copies and MMAs it
@@ -47,7 +48,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 640;  // 4 control warps, 8 dequantisation warps, 8 epilogue warps
 constexpr int kBM = 128;      // weight rows per unit (MMA M)
 constexpr int kBKR = 128;     // int8 K per raw stage (one 128-byte row)
 constexpr int kBK = 64;       // bf16 K per operand stage (one 128-byte row)
@@ -69,7 +70,8 @@ struct TcRing {
 };
 constexpr int kTile = 16384;  // one 128 x 128-byte tile
 constexpr int kScTile = 2048;  // scales of one raw stage: 128 rows x 8 fp16 (a 16-byte aligned window)
-constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12;
+constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12, kEpWarps = 8;
+constexpr int kCpt = 4 / (kDqWarps / 4);  // 16-K chunks per dequantisation thread and operand stage
 
 struct TcParams {
     int K;     // reduction length (d_model for gate/up, d_ff for down)
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 4);
+            mbar_init(acc_empty + b, kEpWarps);
         }
         mbar_init(&drain_bar, 1);
         s_abort = 0;
@@ -389,8 +391,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
         // ---------------------------------------------------------------- dequantisation
+        // thread = (row r, part pq of the 64-K operand stage: kCpt 16-K chunks);
+        // warp w holds rows of TMEM lane quadrant w % 4
         const int tq = (warp - kDqWarp0) * 32 + lane;
-        const int r = tq & (kBM - 1), hf = tq >> 7;  // row, half (one Q8_0 block) of each 64-K operand stage
+        const int r = tq & (kBM - 1), pq = tq >> 7;
         uint32_t rc = 0, ac = 0;
         for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
             bool ok = true;
@@ -400,41 +404,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                for (int j = 0; j < 2 && ok; ++j) {
-                    const int s = ac % AS;
-                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                // both operand stages of this raw stage at once: all their TMEM
+                // stores in flight before one wait
+                const int s0 = ac % AS, s1 = (ac + 1) % AS;
+                if (!tc_wait(ab_empty + s0, ((ac / AS) & 1) ^ 1, p.status, &s_abort) ||
+                    !tc_wait(ab_empty + s1, (((ac + 1) / AS) & 1) ^ 1, p.status, &s_abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int s = j ? s1 : s0;
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
                         const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
-                        // this thread's block 4kr + 2j + hf, from the stage's scale window
                         const __half* sc = reinterpret_cast<const __half*>(Ss + (rs * NMAT + mat) * kScTile);
-                        const float d = __half2float(sc[r * 8 + ((4 * kr) & 7) + 2 * j + hf]);
+                        // this thread's block (4kr + 2j + chunk / 2), from the stage's scale window
+                        const float d =
+                            __half2float(sc[r * 8 + ((4 * kr) & 7) + 2 * j + (pq * kCpt) / 2]);
                         const f32x2 dd = f2_pack(d, d);
                         const f32x2 cc = f2_pack(-32896.0f * d, -32896.0f * d);
-                        uint32_t v[16];  // this thread's row: 32 bf16 (K half hf of the 64-K stage)
+                        uint32_t v[8 * kCpt];  // this thread's row: 16 * kCpt bf16 of the 64-K stage
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + 2 * hf + i));
+                        for (int i = 0; i < kCpt; ++i) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + pq * kCpt + i));
                             uint4 o0, o1;
                             dequant16(q, dd, cc, o0, o1);
                             v[8 * i + 0] = o0.x, v[8 * i + 1] = o0.y, v[8 * i + 2] = o0.z, v[8 * i + 3] = o0.w;
                             v[8 * i + 4] = o1.x, v[8 * i + 5] = o1.y, v[8 * i + 6] = o1.z, v[8 * i + 7] = o1.w;
                         }
-                        // TMEM lane = weight row (this warp's lane quadrant), 16 columns = 32 bf16
-                        tmem_st16(tmem + ((uint32_t)(r & ~31) << 16) + kAcol0 +
-                                      (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS + 16 * hf,
-                                  v);
+                        // TMEM lane = weight row (this warp's lane quadrant), 8 columns = 16 bf16 per chunk
+                        tmem_st<8 * kCpt>(tmem + ((uint32_t)(r & ~31) << 16) + kAcol0 +
+                                              (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS + 8 * kCpt * pq,
+                                          v);
                     }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(a_full + s);
-                    ++ac;
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(a_full + s0);
+                    mbar_arrive(a_full + s1);
+                }
+                ac += 2;
                 if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty + rs);
@@ -445,37 +458,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp >= kEpWarp0) {
         // ---------------------------------------------------------------- epilogue
-        const int ew = warp - kEpWarp0;   // == warp % 4: TMEM lanes 32*ew .. 32*ew+31
-        const int row = ew * 32 + lane;   // weight row within the unit
-        const int et = ew * 32 + lane;    // pair slot staged by this thread
+        // kEpWarps warps: warp % 4 picks the TMEM lane quadrant (weight rows),
+        // ep_half = which 16-column chunks (tokens) of the accumulator
+        const int ew = warp % 4;
+        const int ep_half = (warp - kEpWarp0) / 4;
+        const int row = ew * 32 + lane;                 // weight row within the unit
+        const int et = (warp - kEpWarp0) * 32 + lane;  // pair slot staged by this thread (if < kBN)
+        constexpr int kEpThreads = kEpWarps * 32;
         uint32_t uc = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
-            // the four epilogue warps leave together or not at all: they meet
-            // at named barrier 2 below, so one warp leaving alone would strand
+            // the epilogue warps leave together or not at all: they meet at
+            // named barrier 2 below, so one warp leaving alone would strand
             // the others there
-            if (!named_bar_and(2, 128, !s_abort)) break;
+            if (!named_bar_and(2, kEpThreads, !s_abort)) break;
             const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
             if (EPI == 1) {
-                int tok = -1;
-                float w = 0.f;
-                if (et < U.nv) {
-                    const int pp = U.p0 + et;
-                    const int t = __ldcg(p.pair_tok + pp), sl = __ldcg(p.pair_slot + pp);
-                    if (t >= 0 && t < p.T && sl >= 0 && sl < p.k) {
-                        tok = t;
-                        w = __ldcg(p.wts + (size_t)t * p.k + sl);
+                if (et < kBN) {
+                    int tok = -1;
+                    float w = 0.f;
+                    if (et < U.nv) {
+                        const int pp = U.p0 + et;
+                        const int t = __ldcg(p.pair_tok + pp), sl = __ldcg(p.pair_slot + pp);
+                        if (t >= 0 && t < p.T && sl >= 0 && sl < p.k) {
+                            tok = t;
+                            w = __ldcg(p.wts + (size_t)t * p.k + sl);
+                        }
                     }
+                    s_ep_tok[et] = tok;
+                    s_ep_w[et] = w;
                 }
-                s_ep_tok[et] = tok;
-                s_ep_w[et] = w;
-                named_bar(2, 128);
+                named_bar(2, kEpThreads);
             }
             const int buf = uc % NBUF;
             const bool landed = tc_wait(acc_full + buf, (uc / NBUF) & 1, p.status, &s_abort);
-            if (!named_bar_and(2, 128, landed)) break;  // a timeout in any epilogue warp ends all four
+            if (!named_bar_and(2, kEpThreads, landed)) break;  // a timeout in any epilogue warp ends them all
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + buf * NMAT * kBN;
-            for (int c0 = 0; c0 < U.N; c0 += 16) {
+            for (int c0 = 16 * ep_half; c0 < U.N; c0 += 16 * (kEpWarps / 4)) {
                 float g[16], v[16];
                 tmem_ld16(tbase + c0, g);
                 if (NMAT == 2) tmem_ld16(tbase + kBN + c0, v);
@@ -497,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             tc_fence_before();
-            named_bar(2, 128);  // every epilogue thread is done with this buffer and the staged pairs
+            named_bar(2, kEpThreads);  // every epilogue thread is done with this buffer and the staged pairs
             if (lane == 0) mbar_arrive(acc_empty + buf);
         }
     }
