@@ -324,7 +324,7 @@ def workload_config(wl, args, rot=None):
 
 def expert_path_name(wl, tc_path: bool) -> str:
     if tc_path:
-        return "moe_expert_ffn_q8 (tcgen05 gate/up + down, Q8_0 dequant fused, combine fused)"
+        return f"moe_expert_ffn_q8 (tcgen05 gate/up + down, {fmt_name(wl)} dequant fused, combine fused)"
     return f"moe_expert_ffn_q8 (gate/up + down, {fmt_name(wl)} fused, combine fused)"
 
 
@@ -501,7 +501,7 @@ def measure_layer(wl, args, ws, rank, dev, sampler, rot: int, steps: int, warmup
         fused_ms = ms_local / steps
         step_alg0 = float(np.mean([step_bytes[i % R] for i in range(steps)]))
         fa = step_alg0 / (fused_ms / 1e3) / 1e9
-        kname = "decode_fused_kernel" if wl.wfmt == "q4" else "decode_split_kernel"
+        kname = "decode_split_kernel"
         roofline = {"kernel": f"{kname} (whole layer: router, top-k, bucketing, {fmt_name(wl)} "
                               "gate/up + down, combine; one cooperative launch)",
                     "bound": "hbm", "achieved": fa, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -785,6 +785,8 @@ def measure_stack(wl, args, ws, rank, dev, sampler, sw: StackWeights, steps: int
 # workload of the metric as a sub-record of the same line.
 SUITE_LAYERS = ["decode_t64_zipf", "prefill_t768", "prefill_t1024", "prefill_t2048_mb1024", "prefill_t2048"]
 SUITE_STACKS = ["stack48_t1", "stack48_t64", "stack48_t1024"]
+# the 4-bit expert format (Q4_0) at the same geometry, beside its Q8_0 rows
+SUITE_Q4 = ["decode_t1_q4", "decode_t64_zipf_q4", "prefill_t1024_q4"]
 
 
 def run_ours(args, ws, rank, local):
@@ -809,7 +811,7 @@ def run_ours(args, ws, rank, local):
         if args.workload is None and not args.headline_only:
             subs = {}
             sub_cpu = args.sub_cpu_budget if keep_cpu else 0.0
-            for n in SUITE_LAYERS:
+            for n in SUITE_LAYERS + SUITE_Q4:
                 torch.cuda.empty_cache()
                 subs[n] = measure_layer(synth.WORKLOADS[n], args, ws, rank, dev, sampler, args.sub_rot,
                                         args.steps, args.warmup, sub_cpu)
@@ -821,9 +823,9 @@ def run_ours(args, ws, rank, local):
             del sw
             torch.cuda.empty_cache()
             line["workloads"] = subs
-            line["workloads_note"] = ("every workload of the metric, measured in this run with the same K / W "
-                                      f"(the stacks with K/4 steps); value and ms_per_step above are "
-                                      f"{name}'s")
+            line["workloads_note"] = ("every workload of the metric, and the Q4_0 expert format at three of "
+                                      "them, measured in this run with the same K / W (the stacks with K/4 "
+                                      f"steps); value and ms_per_step above are {name}'s")
         line["bench_wall_s"] = time.time() - t_start
     finally:
         sampler.stop()

@@ -88,14 +88,16 @@ extern "C" {
 
 /* ---- expert-input precision ------------------------------------------ */
 #define MOE_ACT_F32 0  /* fp32 activations, CUDA-core contraction (decode) */
-#define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill); batches
-                          of fewer than 128 pairs, or dimensions not multiples of 128, run the
-                          fp32 path (more accurate, and memory-bound at that size anyway) */
+#define MOE_ACT_BF16 1 /* bf16 activations and weights on tcgen05 tensor cores (prefill), Q8_0 or
+                          Q4_0; batches of fewer than 128 pairs, or d_model / d_ff not multiples
+                          of 256, run the fp32 path (more accurate, and memory-bound at that
+                          size anyway) */
 
 /* ---- expert weight formats (moe_layer_w.wfmt) ------------------------- */
 #define MOE_WFMT_Q8_0 0 /* every path */
 #define MOE_WFMT_Q4_0 1 /* fp32 lane-per-row kernels, any T; needs d_model % 512 == 0 and d_ff a
-                           multiple of 256 (else MOE_ERR_UNSUPPORTED); MOE_ACT_BF16 runs them too */
+                           multiple of 256 (else MOE_ERR_UNSUPPORTED); MOE_ACT_BF16 at 128+ pairs:
+                           the tensor-core kernels (d_model, d_ff multiples of 256) */
 
 /* ---- flags ----------------------------------------------------------- */
 #define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */

@@ -55,11 +55,13 @@ bool valid_geometry(const moe_layer_w* w) {
     return w->wfmt == MOE_WFMT_Q8_0 || w->wfmt == MOE_WFMT_Q4_0;
 }
 
-// Whether launch_ffn has a kernel for this call: Q4_0 experts run only on
-// the lane-per-row kernels; an arena slot map only on the kernels that
-// resolve it (lane-per-row, streaming, tensor-core), not on the fallback.
+// Whether launch_ffn has a kernel for this call: Q4_0 experts run on the
+// lane-per-row kernels, or with bf16 activations on the tensor-core kernels;
+// an arena slot map only on the kernels that resolve it (lane-per-row,
+// streaming, tensor-core), not on the fallback.
 bool ffn_supported(const moe_layer_w* w, int T, int act) {
-    if (w->wfmt == MOE_WFMT_Q4_0) return ffn_rows_supported(*w, T > 0 ? T : 1);
+    if (w->wfmt == MOE_WFMT_Q4_0)
+        return (act == MOE_ACT_BF16 && ffn_tc_supported(*w, T)) || ffn_rows_supported(*w, T > 0 ? T : 1);
     if (!w->expert_slot) return true;
     return (act == MOE_ACT_BF16 && ffn_tc_supported(*w, T)) || ffn_rows_supported(*w, T) ||
            (ffn_stream_supported(*w) && ffn_stream_fits(*w, T > 0 ? T : 1));
@@ -111,20 +113,21 @@ int check_device() {
 // more accurate and memory-bound anyway); fp32 -> for 3+ tokens the
 // lane-per-row kernels, for 1-2 tokens the streaming kernels, where the
 // geometry allows; the per-expert-CTA kernels otherwise.  Q4_0 weights: the
-// lane-per-row kernels for every T (the callers have checked the geometry).
+// tensor-core kernels likewise, else the lane-per-row kernels for every T
+// (the callers have checked the geometry).
 cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, const int32_t* offsets,
                        const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse, float* out,
                        int residual, char* ws, const WsLayout& L, int32_t* status, cudaStream_t s,
                        int reuse_order = 0) {
     float* h = reinterpret_cast<float*>(ws + L.h);
-    if (w.wfmt != MOE_WFMT_Q8_0) {
-        if (!ffn_rows_supported(w, T)) return cudaErrorNotSupported;
-        return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
-    }
     if (act == MOE_ACT_BF16 && ffn_tc_supported(w, T))
         return launch_ffn_tc(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual,
                              reinterpret_cast<__nv_bfloat16*>(ws + L.xb), reinterpret_cast<__nv_bfloat16*>(h),
                              status, reuse_order, s);
+    if (w.wfmt != MOE_WFMT_Q8_0) {
+        if (!ffn_rows_supported(w, T)) return cudaErrorNotSupported;
+        return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
+    }
     if (ffn_rows_supported(w, T))
         return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
     if (ffn_stream_supported(w) && ffn_stream_fits(w, T))

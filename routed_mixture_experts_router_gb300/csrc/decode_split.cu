@@ -1,6 +1,6 @@
 // The whole MoE layer for one or two decode tokens in ONE cooperative launch
 // with a single grid-wide exchange: router GEMV -> top-k -> bucketing ->
-// gate/up + SwiGLU -> down + weighted combine, Q8_0 experts ("router ->
+// gate/up + SwiGLU -> down + weighted combine, Q8_0 or Q4_0 experts ("router ->
 // resident expert -> combine -> next layer", amalgafy.com/technical-overview,
 // "Warm target path").
 //
@@ -11,13 +11,14 @@
 //   1. CTA b computes router logit b (its 8 KB router row is bulk-copied into
 //      shared memory at launch) and publishes it as one 64-bit word tagged
 //      with this launch, after initialising its slice of the output
-//      (out = residual ? x : 0); every CTA also publishes a tagged presence
-//      word.  Every CTA reads all the words until each carries its tag, then
-//      ranks the logits itself (top-k, weights, active experts).  The tag is
-//      a launch counter in the workspace, read by every CTA at its start and
-//      bumped by CTA 0 once all presence words are in (so every CTA has read
-//      it): nothing needs clearing between launches, and words of earlier
-//      launches carry other tags whatever the workspace held at first.
+//      (out = residual ? x : 0); a CTA without a router row publishes a
+//      tagged word with no logit (its presence).  Every CTA reads all the
+//      words until each carries its tag -- the logits arrive with them --
+//      then ranks the logits itself (top-k, weights, active experts).  The
+//      tag is a launch counter in the workspace, read by every CTA at its
+//      start and bumped by CTA 0 once every word is in (so every CTA has
+//      read it): nothing needs clearing between launches, and words of
+//      earlier launches carry other tags whatever the workspace held.
 //   2. The routed (expert, feature) units are cut into equal 16-aligned
 //      ranges, one per CTA.  A CTA streams the gate and up rows of its
 //      features (1-D bulk copies; h = silu(g) * u kept in shared memory) and
@@ -52,10 +53,10 @@ constexpr int kSpNST = 3;                     // ring stages
 constexpr int kSpBoxScCols = 16;              // down scale box: fp16 scales per row
 constexpr int kSpMaxChunks = 9;               // down window: 16-column chunks (box width 16 * odd)
 constexpr int kSpWin = kSpMaxChunks * 16;     // h window per segment
-constexpr int kSpMaxT = 2;
+constexpr int kSpMaxT = 2;                    // tokens (the word layout below assumes at most two)
 constexpr int kSpMaxP = kSpMaxT * 16;         // pairs: one warp's lanes hold them
 constexpr int kSpMaxRows = 2;                 // router rows per CTA (E <= 2 * grid)
-constexpr int kSpRankSplit = 3;               // threads per top-k candidate (at most)
+constexpr int kSpRankSplit = 4;               // threads per top-k candidate (at most)
 constexpr int kSpMaxGrid = 1024;              // CTAs (SMs) a launch may use: presence words in the workspace
 
 struct SplitParams {
@@ -71,7 +72,8 @@ struct SplitParams {
     const int8_t* uqs;
     const uint16_t* ud;
     float* out;                   // [T][dm]
-    unsigned long long* lgw;      // [T*E + grid] words: launch tag << 32 | logit bits, then one presence word per CTA
+    unsigned long long* lgw;      // [T][max(E, grid)] words: launch tag << 32 | logit bits (slot e: expert e;
+                                  // slots >= E of token 0: presence words of the CTAs without a router row)
     unsigned int* epoch;          // launch counter (workspace; any start value), its value is this launch's tag
     int32_t* idx_out;             // [T][k] or null
     float* wts_out;               // [T][k] or null
@@ -99,22 +101,22 @@ __device__ __forceinline__ bool sp_wait(uint64_t* bar, uint32_t parity, volatile
     }
 }
 
-// acc[t] += (the 16 weights of one 16-byte chunk, q * d exactly) . x_t, the
-// weights dequantised four at a time and used at once (few live registers):
-// byte u = q + 128 goes into the mantissa of 2^15 and one fma with
-// c = -(2^15 + 128) d gives q d exactly (see dequant16).  xt[t][m * st] is
-// the float4 of x_t matching word m of the chunk.  acc[t][0] collects the
-// even pairs of every chunk, acc[t][1] the odd pairs.
+// acc[t] += (16 weights (u - c0) * d, exactly) . x_t for 16 unsigned bytes u
+// (four words), the weights dequantised four at a time and used at once (few
+// live registers): u goes into the mantissa of 2^15 and one fma with
+// c = -(2^15 + c0) d gives (u - c0) d exactly (see dequant16; Q8_0: u = q +
+// 128, c0 = 128; Q4_0: u = the nibble, c0 = 8).  xt[t][m * st] is the float4
+// of x_t matching word m.  acc[t][0] collects the even pairs of every chunk,
+// acc[t][1] the odd pairs.
 template <int TT>
-__device__ __forceinline__ void chunk_fma(const uint4 q, float d, const float4* const (&xt)[TT], int st,
-                                          f32x2 (&acc)[TT][2]) {
+__device__ __forceinline__ void chunk_fma_u(const uint32_t (&words)[4], float d, float c0,
+                                            const float4* const (&xt)[TT], int st, f32x2 (&acc)[TT][2]) {
     const f32x2 dd = f2_pack(d, d);
-    const float c = -32896.0f * d;
+    const float c = -(32768.0f + c0) * d;
     const f32x2 cc = f2_pack(c, c);
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const uint32_t u = words[m] ^ 0x80808080u;
+        const uint32_t u = words[m];
         const f32x2 w01 = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
                                          __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
                                  dd, cc);
@@ -130,13 +132,34 @@ __device__ __forceinline__ void chunk_fma(const uint4 q, float d, const float4* 
     }
 }
 
+// Q8_0: one 16-byte chunk of 16 int8 values.
+template <int TT>
+__device__ __forceinline__ void chunk_fma(const uint4 q, float d, const float4* const (&xt)[TT], int st,
+                                          f32x2 (&acc)[TT][2]) {
+    const uint32_t u[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
+    chunk_fma_u<TT>(u, d, 128.0f, xt, st, acc);
+}
+
+// Q4_0: the low (half 0: block values 0..15) or high (half 1: values 16..31)
+// nibbles of one 16-byte block.
+template <int TT>
+__device__ __forceinline__ void chunk_fma_q4(const uint4 q, int half, float d, const float4* const (&xt)[TT], int st,
+                                             f32x2 (&acc)[TT][2]) {
+    const int sh = 4 * half;
+    const uint32_t u[4] = {(q.x >> sh) & 0x0F0F0F0Fu, (q.y >> sh) & 0x0F0F0F0Fu, (q.z >> sh) & 0x0F0F0F0Fu,
+                           (q.w >> sh) & 0x0F0F0F0Fu};
+    chunk_fma_u<TT>(u, d, 8.0f, xt, st, acc);
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float4 v) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                  "f"(v.w)
                  : "memory");
 }
 
-template <int KG, int TT>
+// FMT 0: Q8_0 (a weight row of K values is K bytes); FMT 1: Q4_0 (K / 2
+// bytes: 16-byte blocks of 32 values, low nibbles the first 16).
+template <int KG, int TT, int FMT>
 __global__ void __launch_bounds__(kSpThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dd,
                         SplitParams p) {
@@ -157,6 +180,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     __shared__ uint32_t s_tag;
 
     constexpr int kXTok4 = KG * 4 * 32;  // float4 per staged token
+    constexpr int kCF4 = FMT ? 8 : 4;    // float4 of x per 16-byte weight chunk (one lane's share)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(sp_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char* ring = smem;                                              // [kSpNST][kSpStage]
@@ -200,22 +224,27 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     pdl_wait();  // x (the previous layer's output) and the workspace are ready
     for (int i = threadIdx.x; i < TT * d4; i += kSpThreads) {
         const int t = i / d4, q = i - t * d4;
-        xs[t * kXTok4 + stage_idx<32, 4>(q)] =
+        xs[t * kXTok4 + stage_idx<32, kCF4>(q)] =
             t < T ? __ldcg(reinterpret_cast<const float4*>(p.x) + (size_t)t * d4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // the publishing CTAs (one per router row) initialise out: residual ? x : 0
-    const int npub = E < G ? E : G;
-    if (blockIdx.x < npub) {
-        const int n4 = T * d4, per = (n4 + npub - 1) / npub;
-        for (int i = blockIdx.x * per + threadIdx.x; i < min(n4, (blockIdx.x + 1) * per); i += kSpThreads)
-            reinterpret_cast<float4*>(p.out)[i] =
-                p.residual ? __ldcg(reinterpret_cast<const float4*>(p.x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     __syncthreads();
+    // the CTAs with a router row initialise out = residual ? x : 0, one slice
+    // each, from the staged x; warp 0 alone writes it, and every one of its
+    // lanes fences before the CTA's words are published (below), so whoever
+    // sees those words sees the initialised slice
+    const int npub = E < G ? E : G;
+    if (blockIdx.x < npub && warp == 0) {
+        const int n4 = T * d4, per = (n4 + npub - 1) / npub;
+        for (int i = blockIdx.x * per + lane; i < min(n4, (blockIdx.x + 1) * per); i += 32) {
+            const int t = i / d4, q = i - t * d4;
+            reinterpret_cast<float4*>(p.out)[i] =
+                p.residual ? xs[t * kXTok4 + stage_idx<32, kCF4>(q)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
 
-    // 1. router logits of this CTA's rows (threads split K), published with
-    //    release semantics after the out initialisation above; then every
-    //    CTA collects all E words (acquire)
+    // 1. router logits of this CTA's rows (threads split K), published by
+    //    warp 0 (after its fence); then warp 0 reads every CTA's words until
+    //    all carry this launch's tag, the logits with them
     if (nrows > 0) {
         if (!sp_wait(&rbar, 0, &s_abort)) {
             if (threadIdx.x == 0) {
@@ -232,7 +261,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 const float4 w4 = wr[q];
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
-                    const float4 xv = xs[t * kXTok4 + stage_idx<32, 4>(q)];
+                    const float4 xv = xs[t * kXTok4 + stage_idx<32, kCF4>(q)];
                     acc[t] = fmaf(w4.x, xv.x, fmaf(w4.y, xv.y, fmaf(w4.z, xv.z, fmaf(w4.w, xv.w, acc[t]))));
                 }
             }
@@ -242,43 +271,71 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 if (lane == 0 && warp < kSpNW) s_red[j][t][warp] = sw;
             }
         }
-        __syncthreads();  // partial sums in; this CTA's out initialisation done
-        if (threadIdx.x < nrows * T) {
-            const int j = threadIdx.x / T, t = threadIdx.x - j * T;
-            const int e = blockIdx.x + G * j;
-            float v = 0.f;
-            for (int w2 = 0; w2 < kSpNW; ++w2) v += s_red[j][t][w2];  // fixed order
-            v += p.bias ? __ldg(p.bias + e) : 0.f;
-            // release: the out initialisation (ordered before by the CTA
-            // barrier) is visible to whoever sees this word
-            __threadfence();
-            const unsigned long long word = ((unsigned long long)s_tag << 32) | __float_as_uint(v);
-            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.lgw + (size_t)t * E + e), "l"(word)
-                         : "memory");
-        }
     }
-    // every CTA: its presence word (after its logits, in the same order),
-    // then warp 0 reads the grid's presence words until each carries this
-    // launch's tag (words left by earlier launches carry other tags); then
-    // every CTA has read the tag and published, CTA 0 bumps the launch
-    // counter for the next launch, and the logits are read
-    __syncthreads();
-    if (threadIdx.x == 0)
-        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.lgw + (size_t)T * E + blockIdx.x),
-                     "l"((unsigned long long)s_tag << 32)
-                     : "memory");
+    __syncthreads();  // partial sums in
+    const int NW = E > G ? E : G;  // word slots per token
     if (warp == 0) {
         const uint32_t tag = s_tag;
+        float v = 0.f;
+        const bool pub = lane < nrows * T;
+        if (pub) {
+            const int j = lane / T, t = lane - j * T;
+            for (int w2 = 0; w2 < kSpNW; ++w2) v += s_red[j][t][w2];  // fixed order
+            v += p.bias ? __ldg(p.bias + blockIdx.x + G * j) : 0.f;
+        }
+        __threadfence();  // every lane: its slice of out is visible before any word below
+        __syncwarp();
+        if (pub) {
+            const int j = lane / T, t = lane - j * T;
+            const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(v);
+            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.lgw + (size_t)t * NW + blockIdx.x + G * j),
+                         "l"(word)
+                         : "memory");
+        } else if (nrows == 0 && lane == 0) {
+            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.lgw + blockIdx.x),
+                         "l"((unsigned long long)tag << 32)
+                         : "memory");
+        }
+        // token 0: all NW slots (logits, then presence words); tokens >= 1:
+        // the E logit slots.  A word carrying this launch's tag holds this
+        // launch's logit, so each is stored as soon as it is seen.
+        // (T <= 2: word i is slot i of token 0 for i < NW, else slot i - NW of
+        // token 1; either way lgw[i].)  Each pass issues a batch of loads
+        // before it looks at any of them: one round trip per batch, not one
+        // per word.
+        const int nwords = NW + (T - 1) * E;
+        constexpr int kB = 8;  // words per lane per batch
         const unsigned long long t0 = global_ns();
         for (uint32_t it = 0;; ++it) {
             bool mine = true;
-            for (int i = lane; i < G; i += 32) {
-                unsigned long long v;
-                asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p.lgw + (size_t)T * E + i)
-                             : "memory");
-                mine = mine && (uint32_t)(v >> 32) == tag;
+            for (int base = 0; base < nwords; base += 32 * kB) {
+                unsigned long long w[kB];
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int i = base + 32 * u + lane;
+                    w[u] = 0ull;  // tag 0 is never a launch's tag (tags are odd)
+                    if (i < nwords)
+                        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+                                     : "=l"(w[u])
+                                     : "l"(p.lgw + i)
+                                     : "memory");
+                }
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int i = base + 32 * u + lane;
+                    if (i < nwords) {
+                        const int t = i < NW ? 0 : 1, e = i < NW ? i : i - NW;
+                        const bool ok = (uint32_t)(w[u] >> 32) == tag;
+                        if (ok && e < E) {
+                            const float lv = __uint_as_float((uint32_t)w[u]);
+                            s_lg[t][e] = lv != lv ? -INFINITY : lv;
+                        }
+                        mine = mine && ok;
+                    }
+                }
             }
             if (__all_sync(0xffffffffu, mine)) break;
+            __nanosleep(128);  // back off: every CTA polls the same few lines
             if (s_abort || ((it & 15u) == 15u && global_ns() - t0 > kWaitDeadlineNs)) {
                 if (lane == 0) {
                     flag_status(p.status, MOE_STATUS_TIMEOUT_BIT);
@@ -286,15 +343,9 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 }
                 break;
             }
-            __nanosleep(128);
         }
-        __threadfence();  // acquire side: every CTA's logits and out initialisation are visible from here on
+        __threadfence();  // acquire side: every CTA's out initialisation is visible from here on
         if (blockIdx.x == 0 && lane == 0) __stcg(p.epoch, (tag >> 1) + 1u);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < T * E; i += kSpThreads) {
-        const float lv = __uint_as_float((uint32_t)__ldcg(p.lgw + i));
-        s_lg[i / E][i % E] = lv != lv ? -INFINITY : lv;
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -306,7 +357,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     {
         const int nc = T * E;
         const int S = min(kSpRankSplit, max(1, kSpThreads / nc));
-        const int span = (E + S - 1) / S;
+        const int span = (((E + S - 1) / S) + 3) & ~3;  // a multiple of 4 (vector loads)
         for (int id = threadIdx.x; id < nc * S; id += kSpThreads) {
             const int c = id % nc, part = id / nc;
             const int t = c / E, e = c - t * E;
@@ -314,10 +365,21 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             const float v = row[e];
             const int e0 = part * span, e1 = min(E, e0 + span);
             int r = 0;
+            if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
+#pragma unroll 4
+                for (int e2 = e0; e2 < e1; e2 += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(row + e2);
+                    r += (l4.x > v) | ((l4.x == v) & (e2 < e));
+                    r += (l4.y > v) | ((l4.y == v) & (e2 + 1 < e));
+                    r += (l4.z > v) | ((l4.z == v) & (e2 + 2 < e));
+                    r += (l4.w > v) | ((l4.w == v) & (e2 + 3 < e));
+                }
+            } else {
 #pragma unroll 8
-            for (int e2 = e0; e2 < e1; ++e2) {
-                const float l2 = row[e2];
-                r += (l2 > v) | ((l2 == v) & (e2 < e));
+                for (int e2 = e0; e2 < e1; ++e2) {
+                    const float l2 = row[e2];
+                    r += (l2 > v) | ((l2 == v) & (e2 < e));
+                }
             }
             s_rank[part][c] = r;
         }
@@ -371,7 +433,11 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     //    a multiple of 16 features (at most two experts: a range is no longer
     //    than d_ff); the stage sequence is seg 0 gate/up, seg 0 down boxes,
     //    seg 1 gate/up, seg 1 down boxes
-    const int fcap = kSpStage / (2 * dm + dm / 8);  // gate/up features per stage
+    const int rowb = FMT ? dm / 2 : dm;  // bytes of one gate / up weight row
+    // gate/up features per stage (Q4_0: a multiple of the compute warps, so
+    // that every warp gets the same number of features)
+    const int fcap0 = kSpStage / (2 * rowb + dm / 8);
+    const int fcap = (FMT && fcap0 > kSpNW) ? fcap0 - fcap0 % kSpNW : fcap0;
     const int ndn = dm / BR;                         // down boxes per segment
     if (threadIdx.x == 0) {
         const int F = s_n * f;
@@ -387,8 +453,13 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             sg.local0 = local;
             sg.sbase = ns;
             sg.ngu = (sg.r1 - sg.r0 + fcap - 1) / fcap;
-            for (int t = 0; t < kSpMaxT; ++t) sg.w[t] = 0.f;
-            for (int r = s_beg[a]; r < s_end[a]; ++r) sg.w[s_ptok[r]] = s_pw[r];
+#pragma unroll
+            for (int t = 0; t < kSpMaxT; ++t) {  // a token routes to an expert at most once
+                float wt = 0.f;
+                for (int r = s_beg[a]; r < s_end[a]; ++r)
+                    if (s_ptok[r] == t) wt = s_pw[r];
+                sg.w[t] = wt;
+            }
             s_seg[nseg++] = sg;
             local += sg.r1 - sg.r0;
             ns += sg.ngu + ndn;
@@ -425,19 +496,22 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 if (kind == 0) {
                     const int r = sg.r0 + i * fcap, nf = min(fcap, sg.r1 - r);
                     const size_t row = (size_t)sg.e * f + r;
-                    const uint32_t qb = (uint32_t)nf * dm, sb = (uint32_t)nf * (dm / 16);
+                    const uint32_t qb = (uint32_t)nf * rowb, sb = (uint32_t)nf * (dm / 16);
                     mbar_arrive_expect_tx(full + slot, 2 * (qb + sb));
-                    bulk_g2s(b, p.gqs + row * dm, qb, full + slot);
-                    bulk_g2s(b + (size_t)fcap * dm, p.uqs + row * dm, qb, full + slot);
-                    bulk_g2s(b + (size_t)2 * fcap * dm, reinterpret_cast<const unsigned char*>(p.gd) + row * (dm / 16),
-                             sb, full + slot);
-                    bulk_g2s(b + (size_t)2 * fcap * dm + (size_t)fcap * (dm / 16),
+                    bulk_g2s(b, p.gqs + row * rowb, qb, full + slot);
+                    bulk_g2s(b + (size_t)fcap * rowb, p.uqs + row * rowb, qb, full + slot);
+                    bulk_g2s(b + (size_t)2 * fcap * rowb,
+                             reinterpret_cast<const unsigned char*>(p.gd) + row * (dm / 16), sb, full + slot);
+                    bulk_g2s(b + (size_t)2 * fcap * rowb + (size_t)fcap * (dm / 16),
                              reinterpret_cast<const unsigned char*>(p.ud) + row * (dm / 16), sb, full + slot);
                 } else {
                     const int y = sg.e * dm + i * BR;
                     mbar_arrive_expect_tx(full + slot, BR * (W + 2 * kSpBoxScCols));
+                    // the box starts at the byte of the range's first feature
+                    // (Q4_0: of the block that holds it, 16-byte aligned)
+                    const int bx = FMT ? 16 * (sg.r0 / 32) : sg.r0;
                     for (int r0 = 0; r0 < BR; r0 += p.BRB) {
-                        tma_load_2d(b + r0 * W, &tm_dq, sg.r0, y + r0, full + slot);
+                        tma_load_2d(b + r0 * W, &tm_dq, bx, y + r0, full + slot);
                         tma_load_2d(b + BR * W + r0 * 2 * kSpBoxScCols, &tm_dd, (sg.r0 / 32) & ~7, y + r0, full + slot);
                     }
                 }
@@ -469,26 +543,40 @@ __global__ void __launch_bounds__(kSpThreads, 1)
                 // which computes both of its rows over the whole of K
                 const int r = sg.r0 + i * fcap, nf = min(fcap, sg.r1 - r);
                 const int a2 = sg.local0 + i * fcap;
-                const __half* gsc = reinterpret_cast<const __half*>(b + (size_t)2 * fcap * dm);
-                const __half* usc = reinterpret_cast<const __half*>(b + (size_t)2 * fcap * dm + (size_t)fcap * (dm / 16));
+                const __half* gsc = reinterpret_cast<const __half*>(b + (size_t)2 * fcap * rowb);
+                const __half* usc =
+                    reinterpret_cast<const __half*>(b + (size_t)2 * fcap * rowb + (size_t)fcap * (dm / 16));
                 for (int j = (warp - a2 % kSpNW + kSpNW) % kSpNW; j < nf; j += kSpNW) {
-                    const unsigned char* gq = b + (size_t)j * dm;
-                    const unsigned char* uq = b + (size_t)(fcap + j) * dm;
+                    const unsigned char* gq = b + (size_t)j * rowb;
+                    const unsigned char* uq = b + (size_t)(fcap + j) * rowb;
                     f32x2 accg[TT][2], accu[TT][2];
 #pragma unroll
                     for (int t = 0; t < TT; ++t) accg[t][0] = accg[t][1] = accu[t][0] = accu[t][1] = 0ull;
 #pragma unroll
-                    for (int m = 0; m < KG; ++m) {
+                    for (int m = 0; m < (FMT ? KG / 2 : KG); ++m) {
+                        // 16-byte chunk c of the row: Q8_0 16 values (block c / 2),
+                        // Q4_0 one whole block of 32 (block c)
                         const int c = lane + 32 * m;
                         const uint4 qg = *reinterpret_cast<const uint4*>(gq + c * 16);
                         const uint4 qu = *reinterpret_cast<const uint4*>(uq + c * 16);
-                        const float sgv = __half2float(gsc[j * (dm / 32) + (c >> 1)]);
-                        const float suv = __half2float(usc[j * (dm / 32) + (c >> 1)]);
+                        const int blk = FMT ? c : c >> 1;
+                        const float sgv = __half2float(gsc[j * (dm / 32) + blk]);
+                        const float suv = __half2float(usc[j * (dm / 32) + blk]);
                         const float4* xt[TT];
 #pragma unroll
-                        for (int t = 0; t < TT; ++t) xt[t] = xs + t * kXTok4 + m * 4 * 32 + lane;
-                        chunk_fma<TT>(qg, sgv, xt, 32, accg);
-                        chunk_fma<TT>(qu, suv, xt, 32, accu);
+                        for (int t = 0; t < TT; ++t) xt[t] = xs + t * kXTok4 + m * kCF4 * 32 + lane;
+                        if (FMT == 0) {
+                            chunk_fma<TT>(qg, sgv, xt, 32, accg);
+                            chunk_fma<TT>(qu, suv, xt, 32, accu);
+                        } else {
+                            const float4* xh[TT];
+#pragma unroll
+                            for (int t = 0; t < TT; ++t) xh[t] = xt[t] + 4 * 32;
+                            chunk_fma_q4<TT>(qg, 0, sgv, xt, 32, accg);
+                            chunk_fma_q4<TT>(qg, 1, sgv, xh, 32, accg);
+                            chunk_fma_q4<TT>(qu, 0, suv, xt, 32, accu);
+                            chunk_fma_q4<TT>(qu, 1, suv, xh, 32, accu);
+                        }
                     }
                     float ga[TT], ua[TT];
 #pragma unroll
@@ -522,11 +610,19 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kSpMaxChunks; ++c) {
                         if (c < sg.nch) {
-                            const uint4 qv = *reinterpret_cast<const uint4*>(qrow + 16 * c);
+                            // features f0 .. f0 + 15 of the range (Q4_0: one half
+                            // of the block that holds them)
+                            const int f0 = sg.r0 + 16 * c;
                             const float4* ht[TT];
 #pragma unroll
                             for (int t = 0; t < TT; ++t) ht[t] = reinterpret_cast<const float4*>(hs + t * kSpWin + 16 * c);
-                            chunk_fma<TT>(qv, __half2float(sc[(sg.r0 + 16 * c) / 32 - sx]), ht, 1, acc);
+                            const float dv = __half2float(sc[f0 / 32 - sx]);
+                            if (FMT == 0) {
+                                chunk_fma<TT>(*reinterpret_cast<const uint4*>(qrow + 16 * c), dv, ht, 1, acc);
+                            } else {
+                                const uint4 qv = *reinterpret_cast<const uint4*>(qrow + 16 * (f0 / 32 - sg.r0 / 32));
+                                chunk_fma_q4<TT>(qv, (f0 >> 4) & 1, dv, ht, 1, acc);
+                            }
                         }
                     }
                     const int o = i * BR + rl;
@@ -611,9 +707,9 @@ int sp_num_sms() {
     return c;
 }
 
-template <int KG, int TT>
+template <int KG, int TT, int FMT>
 cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w& w, cudaStream_t s) {
-    auto kern = decode_split_kernel<KG, TT>;
+    auto kern = decode_split_kernel<KG, TT, FMT>;
     const size_t smem = sp_smem_bytes<KG, TT>(dm);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -622,15 +718,19 @@ cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w&
     if (err != cudaSuccess || per_sm < 1) return cudaErrorInvalidConfiguration;
     const int G = sp_num_sms();  // one CTA per SM, all co-resident (cooperative launch)
     if (G < 1 || G > kSpMaxGrid || (w.E + G - 1) / G > kSpMaxRows) return cudaErrorInvalidConfiguration;
-    // the widest range a CTA can get (every pair on its own expert), in an
-    // odd number of 16-byte chunks so that the lane-per-row reads of a down
-    // box are free of shared-memory bank conflicts; it must not exceed d_ff
-    // (at most two experts per range)
+    // the widest range a CTA can get (every pair on its own expert); its
+    // down box in an odd number of 16-byte chunks so that the lane-per-row
+    // reads of a box are free of shared-memory bank conflicts.  Q8_0: a
+    // chunk per 16 features; Q4_0: a chunk per 32-feature block the range
+    // touches (a 16-aligned range of L features touches at most
+    // L / 32 + 1 blocks).  The range must not exceed d_ff (at most two
+    // experts per range) nor the h window.
     const long long Fmax = (long long)p.T * p.k * f;
     const int Lmax = (int)(16 * ((Fmax + 16LL * G - 1) / (16LL * G)));
-    int nch = Lmax / 16;
+    if (Lmax / 16 > kSpMaxChunks || Lmax > f) return cudaErrorInvalidConfiguration;
+    int nch = FMT ? Lmax / 32 + 1 : Lmax / 16;
     if ((nch & 1) == 0) ++nch;
-    if (nch > kSpMaxChunks || Lmax > f) return cudaErrorInvalidConfiguration;
+    if (nch > kSpMaxChunks) return cudaErrorInvalidConfiguration;
     SplitParams q = p;
     q.W = 16 * nch;
     // down box rows: the most 32-row groups (at most one per compute warp)
@@ -652,7 +752,7 @@ cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w&
         }
     if (q.BRB == 0) return cudaErrorInvalidConfiguration;
     CUtensorMap tq, td;
-    if (!sp_tmap(&tq, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, (uint64_t)w.E * dm, q.W, q.BRB) ||
+    if (!sp_tmap(&tq, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, FMT ? f / 2 : f, (uint64_t)w.E * dm, q.W, q.BRB) ||
         !sp_tmap(&td, w.down.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, f / 32, (uint64_t)w.E * dm, kSpBoxScCols, q.BRB))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -670,11 +770,14 @@ cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w&
 
 }  // namespace
 
-size_t decode_split_words(int T, int E) { return (size_t)T * E + kSpMaxGrid; }
+size_t decode_split_words(int T, int E) { return (size_t)T * (E > kSpMaxGrid ? E : kSpMaxGrid); }
 
 bool decode_split_supported(const moe_layer_w& w, int T) {
-    if (w.wfmt != MOE_WFMT_Q8_0 || w.expert_slot) return false;
-    return T >= 1 && T <= kSpMaxT && T * w.k <= kSpMaxP && w.d_model % 512 == 0 && w.d_model <= 2048 &&
+    if ((w.wfmt != MOE_WFMT_Q8_0 && w.wfmt != MOE_WFMT_Q4_0) || w.expert_slot) return false;
+    // Q4_0: a lane's 16-byte chunk of a gate/up row holds 32 values, so
+    // d_model is a multiple of 1024 (32 lanes x 32)
+    const int dmul = w.wfmt == MOE_WFMT_Q4_0 ? 1024 : 512;
+    return T >= 1 && T <= kSpMaxT && T * w.k <= kSpMaxP && w.d_model % dmul == 0 && w.d_model <= 2048 &&
            w.d_ff % 256 == 0 && w.d_ff <= 8192 && w.E <= MOE_MAX_EXPERTS && sp_encode_fn() != nullptr;
 }
 
@@ -703,13 +806,20 @@ cudaError_t launch_decode_split(const float* x, int T, const moe_layer_w& w, int
     p.offsets_out = offsets_out;
     p.status = status;
     const int dm = w.d_model, f = w.d_ff;
-#define MOE_SPLIT_GO(KG)                                                                                  \
-    return T == 1 ? launch_split<KG, 1>(p, dm, f, w, s) : launch_split<KG, 2>(p, dm, f, w, s)
+#define MOE_SPLIT_GO(KG, FMT)                                                                             \
+    return T == 1 ? launch_split<KG, 1, FMT>(p, dm, f, w, s) : launch_split<KG, 2, FMT>(p, dm, f, w, s)
+    if (w.wfmt == MOE_WFMT_Q4_0) {
+        switch (dm / 512) {
+            case 2: MOE_SPLIT_GO(2, 1);
+            case 4: MOE_SPLIT_GO(4, 1);
+            default: return cudaErrorInvalidConfiguration;
+        }
+    }
     switch (dm / 512) {
-        case 1: MOE_SPLIT_GO(1);
-        case 2: MOE_SPLIT_GO(2);
-        case 3: MOE_SPLIT_GO(3);
-        case 4: MOE_SPLIT_GO(4);
+        case 1: MOE_SPLIT_GO(1, 0);
+        case 2: MOE_SPLIT_GO(2, 0);
+        case 3: MOE_SPLIT_GO(3, 0);
+        case 4: MOE_SPLIT_GO(4, 0);
         default: return cudaErrorInvalidConfiguration;
     }
 #undef MOE_SPLIT_GO

@@ -50,7 +50,7 @@ namespace {
 
 constexpr int kTcThreads = 640;  // 4 control warps, 8 dequantisation warps, 8 epilogue warps
 constexpr int kBM = 128;      // weight rows per unit (MMA M)
-constexpr int kBKR = 128;     // int8 K per raw stage (one 128-byte row)
+constexpr int kBKR = 128;     // bytes of a weight row per raw stage (128 K of Q8_0, 256 K of Q4_0)
 constexpr int kBK = 64;       // bf16 K per operand stage (one 128-byte row)
 constexpr int kBN = 128;      // max tokens per unit (MMA N)
 constexpr int kReuseBand = 4;  // row tiles per band of the reuse-ordering traversal (down projection)
@@ -72,6 +72,7 @@ constexpr int kTile = 16384;  // one 128 x 128-byte tile
 constexpr int kScTile = 2048;  // scales of one raw stage: 128 rows x 8 fp16 (a 16-byte aligned window)
 constexpr int kDqWarp0 = 4, kDqWarps = 8, kEpWarp0 = 12, kEpWarps = 8;
 constexpr int kCpt = 4 / (kDqWarps / 4);  // 16-K chunks per dequantisation thread and operand stage
+static_assert(kCpt == 2, "a dequantisation thread covers one 32-wide block of an operand stage");
 
 struct TcParams {
     int K;     // reduction length (d_model for gate/up, d_ff for down)
@@ -114,18 +115,19 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
     return r;
 }
 
-// 16 int8 (one 16-byte word) times scale d -> 16 bf16 (two 16-byte words),
-// each w = q * d computed exactly in fp32 and then rounded to bf16 (RNE).
-// The byte u = q + 128 is placed in bits 8..15 of the float 2^15, giving
-// v = 32768 + u exactly; one FMA v * d + c with c = -(32768 + 128) * d (exact:
-// a 9-bit integer times an 11-bit fp16 value) yields (u - 128) * d = q * d,
-// whose 19 significant bits are exact, so the FMA's single rounding is exact.
-__device__ __forceinline__ void dequant16(uint4 q, f32x2 dd, f32x2 cc, uint4& o0, uint4& o1) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// 16 unsigned bytes u (one 16-byte word) -> 16 bf16 (two 16-byte words),
+// each w = (u - c0) * d computed exactly in fp32 and then rounded to bf16
+// (RNE); cc = -(32768 + c0) * d.  The byte is placed in bits 8..15 of the
+// float 2^15, giving v = 32768 + u exactly; one FMA v * d + cc then yields
+// (u - c0) * d.  The exact result has at most 19 significant bits (an 8-bit
+// integer times an 11-bit fp16 value) and cc is exact too (a 13-bit integer
+// times d), so the FMA's single rounding changes nothing.
+// Q8_0: u = q + 128 (c0 = 128); Q4_0: u = the nibble n (c0 = 8).
+__device__ __forceinline__ void dequant16_u(const uint32_t (&w)[4], f32x2 dd, f32x2 cc, uint4& o0, uint4& o1) {
     uint32_t r[8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const uint32_t u = w[m] ^ 0x80808080u;
+        const uint32_t u = w[m];
         const f32x2 lo = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
                                         __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
                                 dd, cc);
@@ -140,6 +142,26 @@ __device__ __forceinline__ void dequant16(uint4 q, f32x2 dd, f32x2 cc, uint4& o0
     }
     o0 = make_uint4(r[0], r[1], r[2], r[3]);
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+// Q8_0: 16 int8 values of one block (one 16-byte word), bytes offset by 128.
+__device__ __forceinline__ void dequant16(uint4 q, f32x2 dd, f32x2 cc, uint4& o0, uint4& o1) {
+    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
+    dequant16_u(w, dd, cc, o0, o1);
+}
+
+// Q4_0: one whole block (16 bytes of nibbles, byte j = element j in its low
+// nibble and element j + 16 in its high nibble) -> its 32 values in order:
+// v[0..7] elements 0..15, v[8..15] elements 16..31.
+__device__ __forceinline__ void dequant32_q4(uint4 q, f32x2 dd, f32x2 cc, uint32_t* v) {
+    const uint32_t lo[4] = {q.x & 0x0F0F0F0Fu, q.y & 0x0F0F0F0Fu, q.z & 0x0F0F0F0Fu, q.w & 0x0F0F0F0Fu};
+    const uint32_t hi[4] = {(q.x >> 4) & 0x0F0F0F0Fu, (q.y >> 4) & 0x0F0F0F0Fu, (q.z >> 4) & 0x0F0F0F0Fu,
+                            (q.w >> 4) & 0x0F0F0F0Fu};
+    uint4 a0, a1, b0, b1;
+    dequant16_u(lo, dd, cc, a0, a1);
+    dequant16_u(hi, dd, cc, b0, b1);
+    v[0] = a0.x, v[1] = a0.y, v[2] = a0.z, v[3] = a0.w, v[4] = a1.x, v[5] = a1.y, v[6] = a1.z, v[7] = a1.w;
+    v[8] = b0.x, v[9] = b0.y, v[10] = b0.z, v[11] = b0.w, v[12] = b1.x, v[13] = b1.y, v[14] = b1.z, v[15] = b1.w;
 }
 
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile
@@ -239,7 +261,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int32_t*
     return false;
 }
 
-template <int NMAT, int EPI>
+template <int NMAT, int EPI, int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_s0,
@@ -249,6 +271,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int NBUF = TcRing<NMAT>::NBUF;
     constexpr uint32_t kTmemCols = 512;  // accumulators, then the A operand stages
     constexpr uint32_t kAcol0 = TcRing<NMAT>::ACC_COLS;
+    constexpr int kKR = FMT ? 2 * kBKR : kBKR;  // K per raw stage: 128 bytes of every row
+    constexpr int kOps = kKR / kBK;             // operand stages per raw stage (2 or 4)
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[kRS], raw_empty[kRS], b_full[AS], a_full[AS], ab_empty[AS];
     __shared__ __align__(8) uint64_t acc_full[NBUF], acc_empty[NBUF], drain_bar;
@@ -303,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = s_tmem;
     const int mt = p.rows / kBM;
     const int n_units = s_cb[s_n] * mt;
-    const int kr_n = p.K / kBKR;
+    const int kr_n = p.K / kKR;
 
     if (warp == 0) {
         // ------------------------------------------------- TMA producer: weights
@@ -319,13 +343,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int rs = rc % kRS;
                     if (!tc_wait(raw_empty + rs, ((rc / kRS) & 1) ^ 1, p.status, &s_abort)) break;
                     mbar_arrive_expect_tx(raw_full + rs, NMAT * (kTile + kScTile));
-                    // the stage's 128 K of int8 weights, and eight fp16 scales per
-                    // row (16-byte aligned window) that hold its four blocks
+                    // the stage's 128 bytes of every weight row (Q8_0: 128 K in four
+                    // blocks; Q4_0: 256 K in eight), and a 16-byte aligned window
+                    // of eight fp16 scales per row that holds those blocks
+                    const int sx = FMT ? 8 * kr : (4 * kr) & ~7;
                     tma_load_2d_hint(raw + (rs * NMAT + 0) * kTile, &tm_a0, kr * kBKR, wrow, raw_full + rs, pol);
-                    tma_load_2d(Ss + (rs * NMAT + 0) * kScTile, &tm_s0, (4 * kr) & ~7, wrow, raw_full + rs);
+                    tma_load_2d(Ss + (rs * NMAT + 0) * kScTile, &tm_s0, sx, wrow, raw_full + rs);
                     if (NMAT == 2) {
                         tma_load_2d_hint(raw + (rs * NMAT + 1) * kTile, &tm_a1, kr * kBKR, wrow, raw_full + rs, pol);
-                        tma_load_2d(Ss + (rs * NMAT + 1) * kScTile, &tm_s1, (4 * kr) & ~7, wrow, raw_full + rs);
+                        tma_load_2d(Ss + (rs * NMAT + 1) * kScTile, &tm_s1, sx, wrow, raw_full + rs);
                     }
                     ++rc;
                 }
@@ -340,16 +366,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
                 const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
                 const int nb = (U.N + kBRows - 1) / kBRows;
-                for (int kr = 0; kr < kr_n && !s_abort; ++kr) {
-                    for (int j = 0; j < 2; ++j) {
-                        const int s = ac % AS;
-                        if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
-                        mbar_arrive_expect_tx(b_full + s, nb * kBRows * 128);
-                        for (int bb = 0; bb < nb; ++bb)
-                            tma_load_2d(Bs + s * kTile + bb * kBRows * 128, &tm_b, kr * kBKR + j * kBK,
-                                        U.p0 + bb * kBRows, b_full + s);
-                        ++ac;
-                    }
+                for (int ks = 0; ks < p.K / kBK && !s_abort; ++ks) {
+                    const int s = ac % AS;
+                    if (!tc_wait(ab_empty + s, ((ac / AS) & 1) ^ 1, p.status, &s_abort)) break;
+                    mbar_arrive_expect_tx(b_full + s, nb * kBRows * 128);
+                    for (int bb = 0; bb < nb; ++bb)
+                        tma_load_2d(Bs + s * kTile + bb * kBRows * 128, &tm_b, ks * kBK, U.p0 + bb * kBRows,
+                                    b_full + s);
+                    ++ac;
                 }
             }
             for (uint32_t c = (ac > AS ? ac - AS : 0); c < ac; ++c) mbar_wait(b_full + c % AS, (c / AS) & 1);
@@ -404,50 +428,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                // both operand stages of this raw stage at once: all their TMEM
+                // the raw stage's operand stages two at a time: all their TMEM
                 // stores in flight before one wait
-                const int s0 = ac % AS, s1 = (ac + 1) % AS;
-                if (!tc_wait(ab_empty + s0, ((ac / AS) & 1) ^ 1, p.status, &s_abort) ||
-                    !tc_wait(ab_empty + s1, (((ac + 1) / AS) & 1) ^ 1, p.status, &s_abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int s = j ? s1 : s0;
-#pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat) {
-                        const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
-                        const __half* sc = reinterpret_cast<const __half*>(Ss + (rs * NMAT + mat) * kScTile);
-                        // this thread's block (4kr + 2j + chunk / 2), from the stage's scale window
-                        const float d =
-                            __half2float(sc[r * 8 + ((4 * kr) & 7) + 2 * j + (pq * kCpt) / 2]);
-                        const f32x2 dd = f2_pack(d, d);
-                        const f32x2 cc = f2_pack(-32896.0f * d, -32896.0f * d);
-                        uint32_t v[8 * kCpt];  // this thread's row: 16 * kCpt bf16 of the 64-K stage
-#pragma unroll
-                        for (int i = 0; i < kCpt; ++i) {
-                            const uint4 q = *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * j + pq * kCpt + i));
-                            uint4 o0, o1;
-                            dequant16(q, dd, cc, o0, o1);
-                            v[8 * i + 0] = o0.x, v[8 * i + 1] = o0.y, v[8 * i + 2] = o0.z, v[8 * i + 3] = o0.w;
-                            v[8 * i + 4] = o1.x, v[8 * i + 5] = o1.y, v[8 * i + 6] = o1.z, v[8 * i + 7] = o1.w;
-                        }
-                        // TMEM lane = weight row (this warp's lane quadrant), 8 columns = 16 bf16 per chunk
-                        tmem_st<8 * kCpt>(tmem + ((uint32_t)(r & ~31) << 16) + kAcol0 +
-                                              (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS + 8 * kCpt * pq,
-                                          v);
+                for (int jp = 0; jp < kOps / 2 && ok; ++jp) {
+                    const int s0 = ac % AS, s1 = (ac + 1) % AS;
+                    if (!tc_wait(ab_empty + s0, ((ac / AS) & 1) ^ 1, p.status, &s_abort) ||
+                        !tc_wait(ab_empty + s1, (((ac + 1) / AS) & 1) ^ 1, p.status, &s_abort)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int s = j ? s1 : s0;
+                        const int js = 2 * jp + j;  // operand stage within the raw stage: 64 K, two blocks
+#pragma unroll
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            const unsigned char* rt = raw + (rs * NMAT + mat) * kTile;
+                            const __half* sc = reinterpret_cast<const __half*>(Ss + (rs * NMAT + mat) * kScTile);
+                            // this thread's block of the stage, from the stage's scale window
+                            const float d =
+                                __half2float(sc[r * 8 + (FMT ? 0 : (4 * kr) & 7) + 2 * js + (pq * kCpt) / 2]);
+                            const f32x2 dd = f2_pack(d, d);
+                            const float c = (FMT ? -32776.0f : -32896.0f) * d;  // -(2^15 + 8 or 128) * d
+                            const f32x2 cc = f2_pack(c, c);
+                            uint32_t v[8 * kCpt];  // this thread's row: 16 * kCpt bf16 of the 64-K stage
+                            if (FMT == 0) {
+#pragma unroll
+                                for (int i = 0; i < kCpt; ++i) {
+                                    const uint4 q =
+                                        *reinterpret_cast<const uint4*>(rt + sw128(r, 4 * js + pq * kCpt + i));
+                                    uint4 o0, o1;
+                                    dequant16(q, dd, cc, o0, o1);
+                                    v[8 * i + 0] = o0.x, v[8 * i + 1] = o0.y, v[8 * i + 2] = o0.z;
+                                    v[8 * i + 3] = o0.w, v[8 * i + 4] = o1.x, v[8 * i + 5] = o1.y;
+                                    v[8 * i + 6] = o1.z, v[8 * i + 7] = o1.w;
+                                }
+                            } else {  // one 16-byte chunk = one whole block of 32 values
+                                dequant32_q4(*reinterpret_cast<const uint4*>(rt + sw128(r, 2 * js + pq)), dd, cc, v);
+                            }
+                            // TMEM lane = weight row (this warp's lane quadrant), 8 columns = 16 bf16 per chunk
+                            tmem_st<8 * kCpt>(tmem + ((uint32_t)(r & ~31) << 16) + kAcol0 +
+                                                  (uint32_t)(s * NMAT + mat) * TcRing<NMAT>::A_COLS + 8 * kCpt * pq,
+                                              v);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(a_full + s0);
+                        mbar_arrive(a_full + s1);
+                    }
+                    ac += 2;
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(a_full + s0);
-                    mbar_arrive(a_full + s1);
-                }
-                ac += 2;
                 if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty + rs);
@@ -601,13 +635,13 @@ int tc_num_sms() {
     return n > 0 ? n : 148;
 }
 
-template <int NMAT, int EPI>
+template <int NMAT, int EPI, int FMT>
 cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& s0,
                       const CUtensorMap& s1, const TcParams& p, cudaStream_t s) {
     constexpr int kRS = TcRing<NMAT>::RS;
     constexpr int AS = TcRing<NMAT>::AS;
     const size_t smem = (size_t)(kRS * NMAT + AS) * kTile + (size_t)kRS * NMAT * kScTile + 1024;
-    auto kern = tc_ffn_kernel<NMAT, EPI>;
+    auto kern = tc_ffn_kernel<NMAT, EPI, FMT>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -626,9 +660,10 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
 }  // namespace
 
 bool ffn_tc_supported(const moe_layer_w& w, int T) {
-    // K a multiple of 256: whole 128-K raw stages, and rows of scales (K / 32
-    // fp16) a multiple of 16 bytes, as a tensor map's row pitch must be
-    return w.wfmt == MOE_WFMT_Q8_0 && w.d_model % 256 == 0 && w.d_ff % 256 == 0 && w.d_model % kBM == 0 &&
+    // K a multiple of 256: whole raw stages (128 K of Q8_0, 256 K of Q4_0),
+    // and rows of scales (K / 32 fp16) a multiple of 16 bytes, as a tensor
+    // map's row pitch must be
+    return (w.wfmt == MOE_WFMT_Q8_0 || w.wfmt == MOE_WFMT_Q4_0) && w.d_model % 256 == 0 && w.d_ff % 256 == 0 && w.d_model % kBM == 0 &&
            w.d_ff % kBM == 0 && (long long)T * w.k >= kBN && encode_fn() != nullptr;
 }
 
@@ -654,9 +689,11 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     }
     CUtensorMap tg, tu, td, txb, th, sg, su, sd;
     const uint64_t ns = (uint64_t)weight_slots(w);
-    if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
-        !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dm, ns * f, kBKR, kBM) ||
-        !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, f, ns * dm, kBKR, kBM) ||
+    const int q4 = w.wfmt == MOE_WFMT_Q4_0;
+    const uint64_t rb_gu = q4 ? dm / 2 : dm, rb_dn = q4 ? f / 2 : f;  // bytes per weight row
+    if (!make_tmap(&tg, w.gate.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rb_gu, ns * f, kBKR, kBM) ||
+        !make_tmap(&tu, w.up.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rb_gu, ns * f, kBKR, kBM) ||
+        !make_tmap(&td, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rb_dn, ns * dm, kBKR, kBM) ||
         !make_tmap(&sg, w.gate.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dm / 32, ns * f, 8, kBM, false) ||
         !make_tmap(&su, w.up.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dm / 32, ns * f, 8, kBM, false) ||
         !make_tmap(&sd, w.down.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, f / 32, ns * dm, 8, kBM, false) ||
@@ -679,7 +716,7 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pg.status = status;
     pg.eslot = w.expert_slot;
     pg.nslots = (int)ns;
-    cudaError_t err = launch_tc<2, 0>(tg, tu, txb, sg, su, pg, s);
+    cudaError_t err = q4 ? launch_tc<2, 0, 1>(tg, tu, txb, sg, su, pg, s) : launch_tc<2, 0, 0>(tg, tu, txb, sg, su, pg, s);
     if (err != cudaSuccess) return err;
     TcParams pd = pg;
     pd.K = f;
@@ -689,8 +726,12 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
     pd.h = nullptr;
     pd.out = out_or_ypairs;
     pd.band = (reuse_order && (dm / kBM) % kReuseBand == 0) ? kReuseBand : 0;
-    if (fuse_combine) return launch_tc<1, 1>(td, td, th, sd, sd, pd, s);
-    return launch_tc<1, 2>(td, td, th, sd, sd, pd, s);
+    if (q4) {
+        if (fuse_combine) return launch_tc<1, 1, 1>(td, td, th, sd, sd, pd, s);
+        return launch_tc<1, 2, 1>(td, td, th, sd, sd, pd, s);
+    }
+    if (fuse_combine) return launch_tc<1, 1, 0>(td, td, th, sd, sd, pd, s);
+    return launch_tc<1, 2, 0>(td, td, th, sd, sd, pd, s);
 }
 
 }  // namespace moe

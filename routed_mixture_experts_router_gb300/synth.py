@@ -88,6 +88,7 @@ WORKLOADS = {
     # Q4_0 experts (the 4-bit format of the pages' next stage), decode
     "decode_t1_q4": Workload("decode_t1_q4", 6, 1, 2048, 768, 128, 8, wfmt="q4"),
     "decode_t64_zipf_q4": Workload("decode_t64_zipf_q4", 7, 64, 2048, 768, 128, 8, zipf=True, wfmt="q4"),
+    "prefill_t1024_q4": Workload("prefill_t1024_q4", 8, 1024, 2048, 768, 128, 8, act="bf16", wfmt="q4"),
 }
 
 

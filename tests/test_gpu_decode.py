@@ -1,4 +1,5 @@
-"""The single-launch decode path (one or two tokens, fp32 activations, Q8_0)
+"""The single-launch decode path (one or two tokens, fp32 activations, Q8_0
+or Q4_0 experts)
 against the CPU oracle, through the C ABI: routing bit-exact (near-ties
 counted), outputs within max relative L2 1e-5, at several geometries, with
 and without the residual, tokens sharing experts, repeated calls on one
@@ -23,9 +24,9 @@ def _cuda():
     binding.load()
 
 
-def _wl(name, T, d, f, E, k, zipf):
+def _wl(name, T, d, f, E, k, zipf, wfmt="q8"):
     return synth.custom(name, wid=zlib.crc32(name.encode()) % 10000 + 500, T=T, d_model=d, d_ff=f, E=E, k=k,
-                        zipf=zipf)
+                        zipf=zipf, wfmt=wfmt)
 
 
 def _run(case, residual=False, flags=0, ws=None, x=None):
@@ -71,6 +72,13 @@ GEOMS = [
     ("e256_k16_t2", 2, 2048, 256, 256, 16, True),
     ("e8_k8", 1, 1024, 768, 8, 8, False),         # k == E: every expert, full softmax
     ("k1_t2", 2, 2048, 768, 128, 1, False),
+    # Q4_0 experts: a 16-byte chunk of a row holds a whole 32-value block;
+    # CTA ranges start on 16-feature boundaries, i.e. mid-block
+    ("q4_t1", 1, 2048, 768, 128, 8, False, "q4"),
+    ("q4_t2", 2, 2048, 768, 128, 8, True, "q4"),
+    ("q4_d1024_f512_t2", 2, 1024, 512, 64, 4, True, "q4"),
+    ("q4_e256_k16_t2", 2, 2048, 256, 256, 16, True, "q4"),
+    ("q4_k1", 1, 1024, 256, 16, 1, False, "q4"),
 ]
 
 
@@ -98,7 +106,7 @@ def test_decode_t2_tokens_share_experts():
     assert rel_l2_max(o[:1], o[1:]) < 1e-6
 
 
-@pytest.mark.parametrize("name", ["decode_t1", "stack48_t1"])
+@pytest.mark.parametrize("name", ["decode_t1", "stack48_t1", "decode_t1_q4"])
 def test_decode_any_workspace_bytes(name):
     """Whatever the workspace held before (every byte random, the published
     logit words included), the call gives the same routing and, up to the

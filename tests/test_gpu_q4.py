@@ -1,7 +1,9 @@
 """Q4_0 experts (fp16 scale, 16 bytes of 4-bit values per 32-wide block)
 through the C ABI against the oracle decoding the same blocks.
 
-Q4_0 runs on the lane-per-row kernels for every batch size, so the cases
+Q4_0 with fp32 activations runs on the lane-per-row kernels for every
+batch size (bf16 activations at 128+ pairs take the tensor-core path, tested
+in test_gpu_tc.py), so the cases
 span one and two tokens (which Q8_0 sends elsewhere), the staged-all-tokens
 and per-chunk variants of the gate/up kernel, and 4/8/12-warp down kernels.
 Routing does not depend on the weight format; it is checked again here
@@ -83,11 +85,12 @@ def test_layer_q4_residual():
     _check(make_case(_wl("q4_res", 9, 512, 256, 16, 4, True)), residual=True)
 
 
-def test_layer_q4_bf16_act_runs_fp32():
-    """MOE_ACT_BF16 with Q4_0 weights runs the fp32 kernels: fp32 accuracy
-    against the oracle fed the fp32 inputs, at a size the tensor-core path
-    would otherwise take (256 pairs)."""
-    _check(make_case(_wl("q4_bf16", 32, 1024, 512, 32, 8, False)), act=binding.MOE_ACT_BF16)
+def test_layer_q4_bf16_act_small_batch_runs_fp32():
+    """MOE_ACT_BF16 with Q4_0 weights and fewer than 128 pairs (one MMA
+    tile) runs the fp32 kernels: fp32 accuracy against the oracle fed the
+    fp32 inputs.  (128 pairs or more take the tensor-core path, tested with
+    the other tensor-core cases.)"""
+    _check(make_case(_wl("q4_bf16", 15, 1024, 512, 32, 8, False)), act=binding.MOE_ACT_BF16)
 
 
 def test_q4_differs_from_q8():

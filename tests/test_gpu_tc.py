@@ -49,9 +49,9 @@ def _check(case, tokens=None, flags=0, residual=False):
     return err
 
 
-def _wl(name, T, d, f, E, k, zipf=False):
+def _wl(name, T, d, f, E, k, zipf=False, wfmt="q8"):
     return synth.custom(name, wid=zlib.crc32(name.encode()) % 10000 + 300,
-                        T=T, d_model=d, d_ff=f, E=E, k=k, zipf=zipf, act="bf16")
+                        T=T, d_model=d, d_ff=f, E=E, k=k, zipf=zipf, act="bf16", wfmt=wfmt)
 
 
 @pytest.mark.parametrize("shape", [
@@ -80,7 +80,24 @@ def test_tc_many_tokens_one_expert():
     _check(case)
 
 
-@pytest.mark.parametrize("name", ["prefill_t1024", "prefill_t768", "prefill_t2048"])
+@pytest.mark.parametrize("shape", [
+    ("tc_q4_small", 64, 256, 256, 16, 8, False),     # one 256-K raw stage per row tile
+    ("tc_q4_zipf", 100, 512, 768, 32, 4, True),      # three raw stages of the down projection
+    ("tc_q4_ragged", 37, 1024, 512, 64, 8, False),   # 296 pairs, ragged buckets
+], ids=lambda s: s[0])
+def test_tc_layer_q4(shape):
+    """Q4_0 experts on the tensor-core path (nibbles dequantised into the
+    MMA's A operand): the same bf16 tolerance against the oracle decoding the
+    same Q4_0 blocks."""
+    _check(make_case(_wl(*shape, wfmt="q4")))
+
+
+def test_tc_layer_q4_deterministic_residual():
+    case = make_case(_wl("tc_q4_det", 64, 512, 256, 16, 8, True, wfmt="q4"))
+    _check(case, flags=binding.MOE_FLAG_DETERMINISTIC, residual=True)
+
+
+@pytest.mark.parametrize("name", ["prefill_t1024", "prefill_t768", "prefill_t2048", "prefill_t1024_q4"])
 def test_tc_prefill_full_sampled(name):
     """qwen3_moe geometry: routing for all tokens, outputs on sampled tokens."""
     case = make_case(synth.WORKLOADS[name])
