@@ -95,9 +95,10 @@ extern "C" {
 
 /* ---- expert weight formats (moe_layer_w.wfmt) ------------------------- */
 #define MOE_WFMT_Q8_0 0 /* every path */
-#define MOE_WFMT_Q4_0 1 /* fp32 lane-per-row kernels, any T; needs d_model % 512 == 0 and d_ff a
-                           multiple of 256 (else MOE_ERR_UNSUPPORTED); MOE_ACT_BF16 at 128+ pairs:
-                           the tensor-core kernels (d_model, d_ff multiples of 256) */
+#define MOE_WFMT_Q4_0 1 /* fp32 lane-per-row kernels, any T; needs d_model and d_ff multiples of
+                           256 (else MOE_ERR_UNSUPPORTED); one or two tokens with d_model a multiple
+                           of 1024 (at most 2048): the single-launch decode kernel; MOE_ACT_BF16 at
+                           128+ pairs: the tensor-core kernels */
 
 /* ---- flags ----------------------------------------------------------- */
 #define MOE_FLAG_DETERMINISTIC 1 /* combine by a fixed-order sum instead of atomics */

@@ -29,7 +29,7 @@ SHAPES = [
     ("t12", 12, 1024, 512, 64, 6, True),      # lane-per-row path, per-chunk activations
     ("t2", 2, 2048, 768, 128, 8, False),      # full geometry, two tokens
     ("rows_t6", 6, 1024, 512, 32, 3, False),  # lane-per-row path, all tokens staged at once
-    ("rows_t21", 21, 512, 768, 16, 4, True),  # lane-per-row path, ragged 8-pair chunks, 12-warp down
+    ("rows_t21", 21, 512, 768, 16, 4, True),  # lane-per-row path, ragged 8-pair chunks, 3 K stages per down warp
 ]
 
 

@@ -5,7 +5,8 @@ Q4_0 with fp32 activations runs on the lane-per-row kernels for every
 batch size (bf16 activations at 128+ pairs take the tensor-core path, tested
 in test_gpu_tc.py), so the cases
 span one and two tokens (which Q8_0 sends elsewhere), the staged-all-tokens
-and per-chunk variants of the gate/up kernel, and 4/8/12-warp down kernels.
+and per-chunk variants of the gate/up kernel, and one to three K stages per
+warp in the down kernel (d_ff 256 to 768).
 Routing does not depend on the weight format; it is checked again here
 because each case draws its own router.
 """
@@ -22,10 +23,11 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [
     # name, T, d, f, E, k, zipf
-    ("q4_t1", 1, 512, 256, 16, 4, False),       # 4-warp down
-    ("q4_t2", 2, 1024, 512, 32, 4, True),       # 8-warp down
-    ("q4_t3", 3, 512, 768, 16, 2, False),       # 12-warp down
+    ("q4_t1", 1, 512, 256, 16, 4, False),       # one K stage per down warp
+    ("q4_t2", 2, 1024, 512, 32, 4, True),       # two K stages per down warp
+    ("q4_t3", 3, 512, 768, 16, 2, False),       # three K stages per down warp
     ("q4_t7", 7, 1024, 256, 24, 3, True),       # all tokens staged
+    ("q4_d256", 5, 256, 256, 16, 4, False),     # one K stage per gate/up warp
     ("q4_t21", 21, 512, 768, 16, 4, True),      # per-chunk activations, ragged 8-pair chunks
     ("q4_t64", 64, 1024, 512, 32, 8, False),
     ("q4_t2_full", 2, 2048, 768, 128, 8, False),
@@ -110,7 +112,8 @@ def test_q4_differs_from_q8():
 
 
 def test_q4_unsupported_geometry():
-    """d_model 256 is not a multiple of 512: Q4_0 is refused before any launch."""
+    """d_ff 128 is not a multiple of 256 (the down kernel splits K = d_ff into
+    four 64-wide slices): Q4_0 is refused before any launch."""
     wl = _wl("q4_bad", 3, 256, 128, 8, 2, False)
     case = make_case(wl)
     with pytest.raises(binding.MoeError) as ei:
