@@ -65,6 +65,11 @@ struct SplitParams {
     int W;                        // down box width in bytes (16 * odd, >= every CTA's range)
     int BR;                       // down box rows (a multiple of 32)
     int BRB;                      // rows of one TMA box (BR / BRB boxes per stage; TMA boxes have <= 256 rows)
+    int fcap;                     // gate/up features per ring stage
+    int ndn;                      // down boxes per segment (d_model / BR)
+    // ceil(2^40 / n) for n = d_ff, fcap and 16 * grid: fast_div() divides by
+    // them exactly (the serial scheduling step has no integer divisions)
+    unsigned long long m_f, m_fcap, m_g16;
     const float* Wr;
     const float* bias;
     const int8_t* gqs;
@@ -151,6 +156,14 @@ __device__ __forceinline__ void chunk_fma_q4(const uint4 q, int half, float d, c
     chunk_fma_u<TT>(u, d, 8.0f, xt, st, acc);
 }
 
+// x / n for 0 <= x < 2^24 and m = ceil(2^40 / n): with m n = 2^40 + e,
+// 0 <= e < n, x m / 2^40 = x / n + x e / (n 2^40) and x e < 2^40, so the
+// floor is exact.
+__device__ __forceinline__ int fast_div(int x, unsigned long long m) {
+    return (int)(((unsigned long long)(unsigned)x * m) >> 40);
+}
+unsigned long long fast_div_magic(unsigned n) { return ((1ull << 40) + n - 1) / n; }
+
 __device__ __forceinline__ void red_add_v4(float* addr, float4 v) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                  "f"(v.w)
@@ -223,41 +236,43 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     for (int i = threadIdx.x; i < 2 * TT * kSpWin; i += kSpThreads) hw[i] = 0.f;
     pdl_wait();  // x (the previous layer's output) and the workspace are ready
     for (int i = threadIdx.x; i < TT * d4; i += kSpThreads) {
-        const int t = i / d4, q = i - t * d4;
+        const int t = i >= d4, q = i - t * d4;  // T <= 2
         xs[t * kXTok4 + stage_idx<32, kCF4>(q)] =
             t < T ? __ldcg(reinterpret_cast<const float4*>(p.x) + (size_t)t * d4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    // the CTAs with a router row initialise out = residual ? x : 0, one slice
-    // each, from the staged x; warp 0 alone writes it, and every one of its
-    // lanes fences before the CTA's words are published (below), so whoever
-    // sees those words sees the initialised slice
+    // 1. the CTAs with a router row initialise out = residual ? x : 0, one
+    //    slice each, from the staged x: warp 0 alone writes it and every one
+    //    of its lanes fences at once, while the other warps (the producer
+    //    warp included) compute the router logits of the CTA's rows (threads
+    //    split K).  Warp 0 then publishes the logits -- whoever sees them
+    //    sees the initialised slice -- and reads every CTA's words until all
+    //    carry this launch's tag, the logits with them.
     const int npub = E < G ? E : G;
-    if (blockIdx.x < npub && warp == 0) {
-        const int n4 = T * d4, per = (n4 + npub - 1) / npub;
-        for (int i = blockIdx.x * per + lane; i < min(n4, (blockIdx.x + 1) * per); i += 32) {
-            const int t = i / d4, q = i - t * d4;
-            reinterpret_cast<float4*>(p.out)[i] =
-                p.residual ? xs[t * kXTok4 + stage_idx<32, kCF4>(q)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp == 0) {
+        if (blockIdx.x < npub) {
+            const int n4 = T * d4, per = (n4 + npub - 1) / npub;
+            for (int i = blockIdx.x * per + lane; i < min(n4, (blockIdx.x + 1) * per); i += 32) {
+                const int t = i >= d4, q = i - t * d4;  // T <= 2
+                reinterpret_cast<float4*>(p.out)[i] =
+                    p.residual ? xs[t * kXTok4 + stage_idx<32, kCF4>(q)] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-    }
-
-    // 1. router logits of this CTA's rows (threads split K), published by
-    //    warp 0 (after its fence); then warp 0 reads every CTA's words until
-    //    all carry this launch's tag, the logits with them
-    if (nrows > 0) {
+        __threadfence();  // every lane: its slice of out is visible before any word of this CTA
+    } else if (nrows > 0) {
         if (!sp_wait(&rbar, 0, &s_abort)) {
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 32) {
                 flag_status(p.status, MOE_STATUS_TIMEOUT_BIT);
                 s_abort = 1;
             }
         }
+        const int gw = warp - 1;  // 0 .. kSpNW - 1 (warps 1 .. kSpNW, the producer warp last)
         for (int j = 0; j < nrows; ++j) {
             const float4* wr = reinterpret_cast<const float4*>(ring) + (size_t)j * d4;
             float acc[TT];
 #pragma unroll
             for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-            for (int q = threadIdx.x; q < d4 && warp < kSpNW; q += kSpNW * 32) {
+            for (int q = threadIdx.x - 32; q < d4; q += kSpNW * 32) {
                 const float4 w4 = wr[q];
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
                 const float sw = warp_sum(acc[t]);
-                if (lane == 0 && warp < kSpNW) s_red[j][t][warp] = sw;
+                if (lane == 0) s_red[j][t][gw] = sw;
             }
         }
     }
@@ -279,14 +294,12 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         float v = 0.f;
         const bool pub = lane < nrows * T;
         if (pub) {
-            const int j = lane / T, t = lane - j * T;
+            const int j = T == 2 ? lane >> 1 : lane, t = lane - j * T;
             for (int w2 = 0; w2 < kSpNW; ++w2) v += s_red[j][t][w2];  // fixed order
             v += p.bias ? __ldg(p.bias + blockIdx.x + G * j) : 0.f;
         }
-        __threadfence();  // every lane: its slice of out is visible before any word below
-        __syncwarp();
         if (pub) {
-            const int j = lane / T, t = lane - j * T;
+            const int j = T == 2 ? lane >> 1 : lane, t = lane - j * T;
             const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(v);
             asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.lgw + (size_t)t * NW + blockIdx.x + G * j),
                          "l"(word)
@@ -355,25 +368,31 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     //    a permutation (ties to the lower id); each candidate's scan is split
     //    over S threads whose partial counts are summed in a fixed order.
     {
+        // (no integer division on this serial path: T <= 2, S <= 4)
         const int nc = T * E;
-        const int S = min(kSpRankSplit, max(1, kSpThreads / nc));
-        const int span = (((E + S - 1) / S) + 3) & ~3;  // a multiple of 4 (vector loads)
+        const int S = 4 * nc <= kSpThreads ? 4 : 3 * nc <= kSpThreads ? 3 : 2 * nc <= kSpThreads ? 2 : 1;
+        static_assert(kSpRankSplit == 4, "split cases below");
+        const int per = S == 4 ? (E + 3) >> 2 : S == 3 ? (E + 2) / 3 : S == 2 ? (E + 1) >> 1 : E;
+        const int span = (per + 3) & ~3;  // a multiple of 4 (vector loads)
         for (int id = threadIdx.x; id < nc * S; id += kSpThreads) {
-            const int c = id % nc, part = id / nc;
-            const int t = c / E, e = c - t * E;
+            const int part = (id >= nc) + (id >= 2 * nc) + (id >= 3 * nc);
+            const int c = id - part * nc;
+            const int t = c >= E, e = c - t * E;
             const float* row = s_lg[t];
             const float v = row[e];
             const int e0 = part * span, e1 = min(E, e0 + span);
             int r = 0;
             if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent counts
 #pragma unroll 4
                 for (int e2 = e0; e2 < e1; e2 += 4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(row + e2);
-                    r += (l4.x > v) | ((l4.x == v) & (e2 < e));
-                    r += (l4.y > v) | ((l4.y == v) & (e2 + 1 < e));
-                    r += (l4.z > v) | ((l4.z == v) & (e2 + 2 < e));
-                    r += (l4.w > v) | ((l4.w == v) & (e2 + 3 < e));
+                    r0 += (l4.x > v) | ((l4.x == v) & (e2 < e));
+                    r1 += (l4.y > v) | ((l4.y == v) & (e2 + 1 < e));
+                    r2 += (l4.z > v) | ((l4.z == v) & (e2 + 2 < e));
+                    r3 += (l4.w > v) | ((l4.w == v) & (e2 + 3 < e));
                 }
+                r = (r0 + r1) + (r2 + r3);
             } else {
 #pragma unroll 8
                 for (int e2 = e0; e2 < e1; ++e2) {
@@ -388,7 +407,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             int r = 0;
             for (int part = 0; part < S; ++part) r += s_rank[part][c];
             if (r < k) {
-                const int t = c / E;
+                const int t = c >= E;  // T <= 2
                 s_idx[t * k + r] = c - t * E;
                 s_val[t * k + r] = s_lg[t][c - t * E];
             }
@@ -405,7 +424,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         const bool lead = lane < P && __ffs(same) - 1 == lane;
         const uint32_t leads = __ballot_sync(0xffffffffu, lead);
         const uint32_t leads_below = __ballot_sync(0xffffffffu, lead && e2 < e);
-        const int t = q / k;
+        const int t = q >= k;  // T <= 2
         const float v0 = s_val[t * k];
         const float den = warp_sum(lane < k ? expf(s_val[t * k + lane] - v0) : 0.0f);
         const float w = expf(s_val[q] - v0) / den;
@@ -434,17 +453,14 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     //    than d_ff); the stage sequence is seg 0 gate/up, seg 0 down boxes,
     //    seg 1 gate/up, seg 1 down boxes
     const int rowb = FMT ? dm / 2 : dm;  // bytes of one gate / up weight row
-    // gate/up features per stage (Q4_0: a multiple of the compute warps, so
-    // that every warp gets the same number of features)
-    const int fcap0 = kSpStage / (2 * rowb + dm / 8);
-    const int fcap = (FMT && fcap0 > kSpNW) ? fcap0 - fcap0 % kSpNW : fcap0;
-    const int ndn = dm / BR;                         // down boxes per segment
+    const int fcap = p.fcap, ndn = p.ndn;
     if (threadIdx.x == 0) {
         const int F = s_n * f;
-        const int L = 16 * ((F + 16 * G - 1) / (16 * G));
+        const int L = 16 * fast_div(F + 16 * G - 1, p.m_g16);
         const int lo = min(F, (int)blockIdx.x * L), hi = min(F, lo + L);
         int ns = 0, nseg = 0, local = 0;
-        for (int a = lo / f; lo < hi && a <= (hi - 1) / f && nseg < 2; ++a) {
+        const int a_hi = fast_div(hi - 1, p.m_f);
+        for (int a = fast_div(lo, p.m_f); lo < hi && a <= a_hi && nseg < 2; ++a) {
             SpSeg sg;
             sg.e = s_act[a];
             sg.r0 = max(lo, a * f) - a * f;
@@ -452,7 +468,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             sg.nch = (sg.r1 - sg.r0) / 16;
             sg.local0 = local;
             sg.sbase = ns;
-            sg.ngu = (sg.r1 - sg.r0 + fcap - 1) / fcap;
+            sg.ngu = fast_div(sg.r1 - sg.r0 + fcap - 1, p.m_fcap);
 #pragma unroll
             for (int t = 0; t < kSpMaxT; ++t) {  // a token routes to an expert at most once
                 float wt = 0.f;
@@ -751,6 +767,16 @@ cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w&
             break;
         }
     if (q.BRB == 0) return cudaErrorInvalidConfiguration;
+    // gate/up features per stage (Q4_0: a multiple of the compute warps, so
+    // that every warp gets the same number of features)
+    const int rowb = FMT ? dm / 2 : dm;
+    const int fcap0 = kSpStage / (2 * rowb + dm / 8);
+    q.fcap = (FMT && fcap0 > kSpNW) ? fcap0 - fcap0 % kSpNW : fcap0;
+    q.ndn = dm / q.BR;
+    if (q.fcap < 1 || (long long)w.E * f + 16LL * G >= (1LL << 24)) return cudaErrorInvalidConfiguration;
+    q.m_f = fast_div_magic((unsigned)f);
+    q.m_fcap = fast_div_magic((unsigned)q.fcap);
+    q.m_g16 = fast_div_magic(16u * (unsigned)G);
     CUtensorMap tq, td;
     if (!sp_tmap(&tq, w.down.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, FMT ? f / 2 : f, (uint64_t)w.E * dm, q.W, q.BRB) ||
         !sp_tmap(&td, w.down.d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, f / 32, (uint64_t)w.E * dm, kSpBoxScCols, q.BRB))
