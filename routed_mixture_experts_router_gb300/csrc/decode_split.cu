@@ -90,7 +90,7 @@ struct SplitParams {
 // aligned), the CTA-local index of its first feature, its first stage and
 // its gate/up stage count.
 struct SpSeg {
-    int e, r0, r1, nch, local0, sbase, ngu;
+    int e, a, r0, r1, nch, local0, sbase, ngu;  // a: index of e among the active experts
     float w[kSpMaxT];  // routing weight of each token for this expert (0 if not routed)
 };
 
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     __shared__ __align__(16) float s_lg[kSpMaxT][MOE_MAX_EXPERTS];
     __shared__ int s_rank[kSpRankSplit][kSpMaxT * MOE_MAX_EXPERTS];
     __shared__ float s_red[kSpMaxRows][kSpMaxT][kSpNW];
-    __shared__ int s_act[MOE_MAX_EXPERTS], s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];
-    __shared__ int s_n;
+    __shared__ int s_beg[MOE_MAX_EXPERTS], s_end[MOE_MAX_EXPERTS];  // pair range of active expert a
+    __shared__ int s_pact[MOE_MAX_EXPERTS];  // active experts in id order (the producer warp's list)
     __shared__ int32_t s_idx[kSpMaxP];
     __shared__ float s_val[kSpMaxP];
     __shared__ int32_t s_ptok[kSpMaxP];
@@ -363,129 +363,49 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     __syncthreads();
     pdl_launch_dependents();
 
-    // 2. top-k, weights, bucketing and the active experts, by every CTA.
-    //    Rank of candidate (t, e) = #{e2 : l > l_e} + #{e2 < e : l == l_e},
-    //    a permutation (ties to the lower id); each candidate's scan is split
-    //    over S threads whose partial counts are summed in a fixed order.
-    {
-        // (no integer division on this serial path: T <= 2, S <= 4)
-        const int nc = T * E;
-        const int S = 4 * nc <= kSpThreads ? 4 : 3 * nc <= kSpThreads ? 3 : 2 * nc <= kSpThreads ? 2 : 1;
-        static_assert(kSpRankSplit == 4, "split cases below");
-        const int per = S == 4 ? (E + 3) >> 2 : S == 3 ? (E + 2) / 3 : S == 2 ? (E + 1) >> 1 : E;
-        const int span = (per + 3) & ~3;  // a multiple of 4 (vector loads)
-        for (int id = threadIdx.x; id < nc * S; id += kSpThreads) {
-            const int part = (id >= nc) + (id >= 2 * nc) + (id >= 3 * nc);
-            const int c = id - part * nc;
-            const int t = c >= E, e = c - t * E;
-            const float* row = s_lg[t];
-            const float v = row[e];
-            const int e0 = part * span, e1 = min(E, e0 + span);
-            int r = 0;
-            if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
-                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent counts
+    // 2. top-k by every CTA.  Rank of candidate (t, e) = #{e2 : l > l_e} +
+    //    #{e2 < e : l == l_e}, a permutation (ties to the lower id); each
+    //    candidate's scan is split over S threads whose partial counts are
+    //    summed in a fixed order.
+    // (no integer division on this serial path: T <= 2, S <= 4)
+    const int nc = T * E;
+    const int S = 4 * nc <= kSpThreads ? 4 : 3 * nc <= kSpThreads ? 3 : 2 * nc <= kSpThreads ? 2 : 1;
+    static_assert(kSpRankSplit == 4, "split cases below");
+    const int per = S == 4 ? (E + 3) >> 2 : S == 3 ? (E + 2) / 3 : S == 2 ? (E + 1) >> 1 : E;
+    const int span = (per + 3) & ~3;  // a multiple of 4 (vector loads)
+    for (int id = threadIdx.x; id < nc * S; id += kSpThreads) {
+        const int part = (id >= nc) + (id >= 2 * nc) + (id >= 3 * nc);
+        const int c = id - part * nc;
+        const int t = c >= E, e = c - t * E;
+        const float* row = s_lg[t];
+        const float v = row[e];
+        const int e0 = part * span, e1 = min(E, e0 + span);
+        int r = 0;
+        if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent counts
 #pragma unroll 4
-                for (int e2 = e0; e2 < e1; e2 += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(row + e2);
-                    r0 += (l4.x > v) | ((l4.x == v) & (e2 < e));
-                    r1 += (l4.y > v) | ((l4.y == v) & (e2 + 1 < e));
-                    r2 += (l4.z > v) | ((l4.z == v) & (e2 + 2 < e));
-                    r3 += (l4.w > v) | ((l4.w == v) & (e2 + 3 < e));
-                }
-                r = (r0 + r1) + (r2 + r3);
-            } else {
+            for (int e2 = e0; e2 < e1; e2 += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(row + e2);
+                r0 += (l4.x > v) | ((l4.x == v) & (e2 < e));
+                r1 += (l4.y > v) | ((l4.y == v) & (e2 + 1 < e));
+                r2 += (l4.z > v) | ((l4.z == v) & (e2 + 2 < e));
+                r3 += (l4.w > v) | ((l4.w == v) & (e2 + 3 < e));
+            }
+            r = (r0 + r1) + (r2 + r3);
+        } else {
 #pragma unroll 8
-                for (int e2 = e0; e2 < e1; ++e2) {
-                    const float l2 = row[e2];
-                    r += (l2 > v) | ((l2 == v) & (e2 < e));
-                }
-            }
-            s_rank[part][c] = r;
-        }
-        __syncthreads();
-        for (int c = threadIdx.x; c < nc; c += kSpThreads) {
-            int r = 0;
-            for (int part = 0; part < S; ++part) r += s_rank[part][c];
-            if (r < k) {
-                const int t = c >= E;  // T <= 2
-                s_idx[t * k + r] = c - t * E;
-                s_val[t * k + r] = s_lg[t][c - t * E];
+            for (int e2 = e0; e2 < e1; ++e2) {
+                const float l2 = row[e2];
+                r += (l2 > v) | ((l2 == v) & (e2 < e));
             }
         }
+        s_rank[part][c] = r;
     }
     __syncthreads();
-    for (int q = warp; q < P && warp < kSpNW; q += kSpNW) {
-        const int e = s_idx[q];
-        const int e2 = lane < P ? s_idx[lane] : 0x7fffffff;
-        const uint32_t lt = __ballot_sync(0xffffffffu, e2 < e);
-        const uint32_t eq = __ballot_sync(0xffffffffu, e2 == e);
-        const uint32_t eq_before = eq & ((1u << q) - 1u);
-        const uint32_t same = __match_any_sync(0xffffffffu, e2);
-        const bool lead = lane < P && __ffs(same) - 1 == lane;
-        const uint32_t leads = __ballot_sync(0xffffffffu, lead);
-        const uint32_t leads_below = __ballot_sync(0xffffffffu, lead && e2 < e);
-        const int t = q >= k;  // T <= 2
-        const float v0 = s_val[t * k];
-        const float den = warp_sum(lane < k ? expf(s_val[t * k + lane] - v0) : 0.0f);
-        const float w = expf(s_val[q] - v0) / den;
-        if (lane == 0) {
-            const int r = __popc(lt) + __popc(eq_before);
-            s_ptok[r] = t;
-            s_pw[r] = w;
-            if (eq_before == 0) {
-                const int a = __popc(leads_below);
-                s_act[a] = e;
-                s_beg[a] = __popc(lt);
-                s_end[a] = __popc(lt) + __popc(eq);
-            }
-            if (q == 0) s_n = __popc(leads);
-            if (blockIdx.x == 0) {
-                if (p.idx_out) p.idx_out[q] = e;
-                if (p.wts_out) p.wts_out[q] = w;
-            }
-        }
-    }
-    if (blockIdx.x == 0 && p.offsets_out) bucket_offsets(s_idx, P, E, kSpThreads, p.offsets_out);
-    __syncthreads();
-
-    // 3. this CTA's range of (active expert, feature) units: equal ranges of
-    //    a multiple of 16 features (at most two experts: a range is no longer
-    //    than d_ff); the stage sequence is seg 0 gate/up, seg 0 down boxes,
-    //    seg 1 gate/up, seg 1 down boxes
     const int rowb = FMT ? dm / 2 : dm;  // bytes of one gate / up weight row
     const int fcap = p.fcap, ndn = p.ndn;
-    if (threadIdx.x == 0) {
-        const int F = s_n * f;
-        const int L = 16 * fast_div(F + 16 * G - 1, p.m_g16);
-        const int lo = min(F, (int)blockIdx.x * L), hi = min(F, lo + L);
-        int ns = 0, nseg = 0, local = 0;
-        const int a_hi = fast_div(hi - 1, p.m_f);
-        for (int a = fast_div(lo, p.m_f); lo < hi && a <= a_hi && nseg < 2; ++a) {
-            SpSeg sg;
-            sg.e = s_act[a];
-            sg.r0 = max(lo, a * f) - a * f;
-            sg.r1 = min(hi, (a + 1) * f) - a * f;
-            sg.nch = (sg.r1 - sg.r0) / 16;
-            sg.local0 = local;
-            sg.sbase = ns;
-            sg.ngu = fast_div(sg.r1 - sg.r0 + fcap - 1, p.m_fcap);
-#pragma unroll
-            for (int t = 0; t < kSpMaxT; ++t) {  // a token routes to an expert at most once
-                float wt = 0.f;
-                for (int r = s_beg[a]; r < s_end[a]; ++r)
-                    if (s_ptok[r] == t) wt = s_pw[r];
-                sg.w[t] = wt;
-            }
-            s_seg[nseg++] = sg;
-            local += sg.r1 - sg.r0;
-            ns += sg.ngu + ndn;
-        }
-        s_nst = s_abort ? 0 : ns;
-        s_nseg = nseg;
-    }
-    __syncthreads();
-    const int nst = s_nst;
-    // stage s -> (segment, kind, index within its kind)
+    // stage s -> (segment, kind, index within its kind); valid once the
+    // producer warp has published the schedule
     auto stage_of = [&](int s, int& seg, int& kind, int& i) {
         seg = (s_nseg > 1 && s >= s_seg[1].sbase) ? 1 : 0;
         i = s - s_seg[seg].sbase;
@@ -495,6 +415,55 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 
     if (warp == kSpNW) {
         // ------------------------------------------------------------ producer
+        // 3. the active experts in id order straight from the ranks (expert
+        //    e is active if some token ranks it below k), this CTA's range of
+        //    (active expert, feature) units -- equal ranges of a multiple of
+        //    16 features, at most two experts -- and its stage list: seg 0
+        //    gate/up, seg 0 down boxes, seg 1 gate/up, seg 1 down boxes.  The
+        //    schedule goes to the compute warps through named barrier 1 and
+        //    the stream starts at once; the routing weights, the bucketing and
+        //    the outputs for the caller are left to the compute warps.
+        int n = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            bool sel = false;
+            if (e < E)
+                for (int t = 0; t < T; ++t) {
+                    int r = 0;
+                    for (int part = 0; part < S; ++part) r += s_rank[part][t * E + e];
+                    sel = sel || r < k;
+                }
+            const uint32_t m = __ballot_sync(0xffffffffu, sel);
+            if (sel) s_pact[n + __popc(m & ((1u << lane) - 1u))] = e;
+            n += __popc(m);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const int F = n * f;
+            const int L = 16 * fast_div(F + 16 * G - 1, p.m_g16);
+            const int lo = min(F, (int)blockIdx.x * L), hi = min(F, lo + L);
+            int ns = 0, nseg = 0, local = 0;
+            const int a_hi = fast_div(hi - 1, p.m_f);
+            for (int a = fast_div(lo, p.m_f); lo < hi && a <= a_hi && nseg < 2; ++a) {
+                SpSeg sg;
+                sg.e = s_pact[a];
+                sg.a = a;
+                sg.r0 = max(lo, a * f) - a * f;
+                sg.r1 = min(hi, (a + 1) * f) - a * f;
+                sg.nch = (sg.r1 - sg.r0) / 16;
+                sg.local0 = local;
+                sg.sbase = ns;
+                sg.ngu = fast_div(sg.r1 - sg.r0 + fcap - 1, p.m_fcap);
+                s_seg[nseg++] = sg;
+                local += sg.r1 - sg.r0;
+                ns += sg.ngu + ndn;
+            }
+            s_nst = s_abort ? 0 : ns;
+            s_nseg = nseg;
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 1, %0;" ::"r"(kSpThreads) : "memory");
+        const int nst = s_nst;
         if (lane == 0) {
             fence_proxy_async_smem();  // the router rows were read through the generic proxy
             int s = 0;
@@ -536,6 +505,63 @@ __global__ void __launch_bounds__(kSpThreads, 1)
             for (int c = (s > kSpNST ? s - kSpNST : 0); c < s; ++c) mbar_wait(full + c % kSpNST, (c / kSpNST) & 1);
         }
     } else {
+        // select, weights, bucketing (the compute warps, 512 threads)
+        constexpr int kCT = kSpNW * 32;
+        for (int c = threadIdx.x; c < nc; c += kCT) {
+            int r = 0;
+            for (int part = 0; part < S; ++part) r += s_rank[part][c];
+            if (r < k) {
+                const int t = c >= E;  // T <= 2
+                s_idx[t * k + r] = c - t * E;
+                s_val[t * k + r] = s_lg[t][c - t * E];
+            }
+        }
+        named_bar(2, kCT);
+        for (int q = warp; q < P; q += kSpNW) {
+            const int e = s_idx[q];
+            const int e2 = lane < P ? s_idx[lane] : 0x7fffffff;
+            const uint32_t lt = __ballot_sync(0xffffffffu, e2 < e);
+            const uint32_t eq = __ballot_sync(0xffffffffu, e2 == e);
+            const uint32_t eq_before = eq & ((1u << q) - 1u);
+            const uint32_t same = __match_any_sync(0xffffffffu, e2);
+            const bool lead = lane < P && __ffs(same) - 1 == lane;
+            const uint32_t leads_below = __ballot_sync(0xffffffffu, lead && e2 < e);
+            const int t = q >= k;  // T <= 2
+            const float v0 = s_val[t * k];
+            const float den = warp_sum(lane < k ? expf(s_val[t * k + lane] - v0) : 0.0f);
+            const float w = expf(s_val[q] - v0) / den;
+            if (lane == 0) {
+                const int r = __popc(lt) + __popc(eq_before);
+                s_ptok[r] = t;
+                s_pw[r] = w;
+                if (eq_before == 0) {
+                    const int a = __popc(leads_below);
+                    s_beg[a] = __popc(lt);
+                    s_end[a] = __popc(lt) + __popc(eq);
+                }
+                if (blockIdx.x == 0) {
+                    if (p.idx_out) p.idx_out[q] = e;
+                    if (p.wts_out) p.wts_out[q] = w;
+                }
+            }
+        }
+        if (blockIdx.x == 0 && p.offsets_out) bucket_offsets(s_idx, P, E, kCT, p.offsets_out);
+        named_bar(2, kCT);                            // pairs in (s_beg, s_end, s_ptok, s_pw)
+        named_bar(1, kSpThreads);                     // the producer's schedule is in
+        if (threadIdx.x == 0) {
+            for (int sg = 0; sg < s_nseg; ++sg) {
+                const int a = s_seg[sg].a;
+#pragma unroll
+                for (int t = 0; t < kSpMaxT; ++t) {  // a token routes to an expert at most once
+                    float wt = 0.f;
+                    for (int r = s_beg[a]; r < s_end[a]; ++r)
+                        if (s_ptok[r] == t) wt = s_pw[r];
+                    s_seg[sg].w[t] = wt;
+                }
+            }
+        }
+        named_bar(2, kCT);
+        const int nst = s_nst;
         // -------------------------------------------------------------- compute
         // After a timeout (`ok` false) the warp walks the remaining stages
         // without waiting or computing.
@@ -665,7 +691,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
 
     // 4. this CTA's partial outputs into out (vector fp32 atomics; out was
     //    initialised before any CTA could pass step 1)
-    if (nst > 0) {
+    if (s_nst > 0) {
         for (int i = threadIdx.x; i < T * d4; i += kSpThreads)
             red_add_v4(p.out + 4 * (size_t)i, reinterpret_cast<const float4*>(ys)[i]);
     }
