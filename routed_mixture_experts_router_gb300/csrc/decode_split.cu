@@ -381,7 +381,21 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         const float v = row[e];
         const int e0 = part * span, e1 = min(E, e0 + span);
         int r = 0;
-        if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
+        if (e1 - e0 == 32 && (e0 & 3) == 0) {  // E = 128 split four ways: eight vector loads, all in flight
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            float4 l[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) l[i] = *reinterpret_cast<const float4*>(row + e0 + 4 * i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e2 = e0 + 4 * i;
+                r0 += (l[i].x > v) | ((l[i].x == v) & (e2 < e));
+                r1 += (l[i].y > v) | ((l[i].y == v) & (e2 + 1 < e));
+                r2 += (l[i].z > v) | ((l[i].z == v) & (e2 + 2 < e));
+                r3 += (l[i].w > v) | ((l[i].w == v) & (e2 + 3 < e));
+            }
+            r = (r0 + r1) + (r2 + r3);
+        } else if (((e0 | e1) & 3) == 0) {  // 16-byte aligned run: vector loads (a broadcast per warp)
             int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent counts
 #pragma unroll 4
             for (int e2 = e0; e2 < e1; e2 += 4) {
@@ -423,18 +437,30 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         //    schedule goes to the compute warps through named barrier 1 and
         //    the stream starts at once; the routing weights, the bucketing and
         //    the outputs for the caller are left to the compute warps.
-        int n = 0;
-        for (int e0 = 0; e0 < E; e0 += 32) {
-            const int e = e0 + lane;
+        // (every rank load of the scan issued before any is used: one
+        // shared-memory round trip, not one per load)
+        constexpr int kJ = MOE_MAX_EXPERTS / 32;
+        bool selj[kJ];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const int e = 32 * j + lane;
+            int r[kSpMaxT][kSpRankSplit];
+#pragma unroll
+            for (int t = 0; t < kSpMaxT; ++t)
+#pragma unroll
+                for (int part = 0; part < kSpRankSplit; ++part)
+                    r[t][part] = (e < E && t < T && part < S) ? s_rank[part][t * E + e] : 0;
             bool sel = false;
-            if (e < E)
-                for (int t = 0; t < T; ++t) {
-                    int r = 0;
-                    for (int part = 0; part < S; ++part) r += s_rank[part][t * E + e];
-                    sel = sel || r < k;
-                }
-            const uint32_t m = __ballot_sync(0xffffffffu, sel);
-            if (sel) s_pact[n + __popc(m & ((1u << lane) - 1u))] = e;
+#pragma unroll
+            for (int t = 0; t < kSpMaxT; ++t)
+                sel = sel || (e < E && t < T && (r[t][0] + r[t][1]) + (r[t][2] + r[t][3]) < k);
+            selj[j] = sel;
+        }
+        int n = 0;
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const uint32_t m = __ballot_sync(0xffffffffu, selj[j]);
+            if (selj[j]) s_pact[n + __popc(m & ((1u << lane) - 1u))] = 32 * j + lane;
             n += __popc(m);
         }
         __syncwarp();
