@@ -58,6 +58,7 @@ constexpr int kSpMaxP = kSpMaxT * 16;         // pairs: one warp's lanes hold th
 constexpr int kSpMaxRows = 2;                 // router rows per CTA (E <= 2 * grid)
 constexpr int kSpRankSplit = 4;               // threads per top-k candidate (at most)
 constexpr int kSpMaxGrid = 1024;              // CTAs (SMs) a launch may use: presence words in the workspace
+constexpr bool kSpEarlyRows = false;          // router rows copied before griddepcontrol.wait
 
 struct SplitParams {
     const float* x;
@@ -206,14 +207,17 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     const int P = T * k, d4 = dm / 4;
     const int W = p.W, BR = p.BR;
     const int G = gridDim.x;
-    // this launch's tag: the launch counter (bumped below once every CTA has
-    // read it), made odd so that zeroed memory never carries it
-    if (threadIdx.x == 0) s_tag = (__ldcg(p.epoch) << 1) | 1u;
-
     // 0. this CTA's router rows (e = blockIdx.x + G * j) start streaming into
     //    the (still idle) ring at once: they do not depend on the previous
-    //    kernel, so the copy overlaps its tail and the staging of x
+    //    kernel, so the copy overlaps its tail (this kernel is launched as a
+    //    programmatic dependent: its CTAs start as the previous kernel's
+    //    leave) and the staging of x
     const int nrows = blockIdx.x < E ? (E - blockIdx.x + G - 1) / G : 0;
+    auto issue_rows = [&]() {
+        mbar_arrive_expect_tx(&rbar, (uint32_t)nrows * dm * 4);
+        for (int j = 0; j < nrows; ++j)
+            bulk_g2s(ring + (size_t)j * dm * 4, p.Wr + (size_t)(blockIdx.x + G * j) * dm, dm * 4, &rbar);
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSpNST; ++s) {
             mbar_init(full + s, 1);
@@ -224,9 +228,7 @@ __global__ void __launch_bounds__(kSpThreads, 1)
         mbar_init(&rbar, 1);
         s_abort = 0;
         fence_barrier_init();
-        mbar_arrive_expect_tx(&rbar, (uint32_t)nrows * dm * 4);
-        for (int j = 0; j < nrows; ++j)
-            bulk_g2s(ring + (size_t)j * dm * 4, p.Wr + (size_t)(blockIdx.x + G * j) * dm, dm * 4, &rbar);
+        if (kSpEarlyRows) issue_rows();
     }
     if (warp == kSpNW && lane == 0) {
         prefetch_tmap(&tm_dq);
@@ -235,6 +237,15 @@ __global__ void __launch_bounds__(kSpThreads, 1)
     for (int i = threadIdx.x; i < TT * dm; i += kSpThreads) ys[i] = 0.f;
     for (int i = threadIdx.x; i < 2 * TT * kSpWin; i += kSpThreads) hw[i] = 0.f;
     pdl_wait();  // x (the previous layer's output) and the workspace are ready
+    // this launch's tag: the launch counter (bumped below once every CTA has
+    // read it), made odd so that zeroed memory never carries it.  Read only
+    // after the previous kernel is complete: a previous launch of this kernel
+    // on the same workspace bumps it, and this launch may start while that
+    // one's last CTAs still run (programmatic dependent launch).
+    if (threadIdx.x == 0) {
+        s_tag = (__ldcg(p.epoch) << 1) | 1u;
+        if (!kSpEarlyRows) issue_rows();
+    }
     for (int i = threadIdx.x; i < TT * d4; i += kSpThreads) {
         const int t = i >= d4, q = i - t * d4;  // T <= 2
         xs[t * kXTok4 + stage_idx<32, kCF4>(q)] =
@@ -838,12 +849,28 @@ cudaError_t launch_split(const SplitParams& p, int dm, int f, const moe_layer_w&
     cfg.blockDim = dim3(kSpThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // cooperative (every CTA resident: the exchange waits on all of them) and
+    // a programmatic dependent of the previous kernel in the stream (its
+    // prologue -- barriers, the router row copy -- overlaps that kernel's
+    // tail; everything that reads what the previous kernel wrote comes after
+    // griddepcontrol.wait).  Where the pair of attributes is refused, the
+    // launch is made cooperative only, and that answer is kept.
+    static std::atomic<int> pdl_ok{1};
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tq, td, q);
+    cfg.numAttrs = pdl_ok.load(std::memory_order_relaxed) ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tq, td, q);
+    if (e != cudaSuccess && cfg.numAttrs == 2 && e != cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        pdl_ok.store(0, std::memory_order_relaxed);
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, tq, td, q);
+    }
+    return e;
 }
 
 }  // namespace
