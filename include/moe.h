@@ -227,10 +227,19 @@ MOE_API int moe_combine(const float* ypairs, const float* wts, const int32_t* po
  *       token or two, where it saves a separate copy.
  * Paths: one or two tokens on the fp32 path without MOE_FLAG_DETERMINISTIC
  * run as ONE cooperative kernel (router, top-k, bucketing, gate/up, down and
- * combine; an 8-byte memset of the workspace's barrier words precedes it);
- * otherwise router, bucketing and the expert kernels (tcgen05 for MOE_ACT_BF16
- * with >= 128 pairs).  Grid barriers and mbarrier waits are bounded
- * (MOE_STATUS_TIMEOUT).
+ * combine) with one grid-wide exchange of launch-tagged words kept in the
+ * workspace: nothing is cleared between calls and any prior workspace
+ * content is safe (shapes that kernel does not take -- d_model not a
+ * multiple of 512, or of 1024 for Q4_0 -- use an older single-launch kernel
+ * whose 8-byte barrier words are cleared by a memset before it, where it
+ * fits, and the separate kernels otherwise).  The kernel is
+ * launched as a programmatic dependent of the previous kernel in the stream:
+ * its blocks may become resident while that kernel's last blocks run, but
+ * everything it reads that a previous kernel may have written (x, the
+ * weights, the workspace) is read after that kernel has completed.
+ * Otherwise router, bucketing and the expert kernels (tcgen05 for
+ * MOE_ACT_BF16 with >= 128 pairs).  Grid exchanges and mbarrier waits are
+ * bounded (MOE_STATUS_TIMEOUT).
  *   act: MOE_ACT_F32 or MOE_ACT_BF16; flags: MOE_FLAG_*
  *   residual: 1 adds x to the output (a residual stream between layers)
  *   idx_out [T][k], wts_out [T][k], offsets_out [E+1]: optional copies of the
