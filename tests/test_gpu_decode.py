@@ -170,3 +170,46 @@ def test_decode_graph_replays_see_new_inputs():
         torch.cuda.synchronize()
         assert torch.equal(idx, ridx), step
         assert rel_l2_max(out.double().cpu().numpy(), ref.double().cpu().numpy()) < 1e-6, step
+
+
+def test_decode_inputs_written_by_the_previous_kernel():
+    """The decode kernel may start while the previous kernel in the stream
+    still runs (programmatic dependent launch): x, the router weights and the
+    bias written by the kernels right before the call must all be the values
+    it uses.  Each step, captured once in a graph, first overwrites them in
+    place (a copy kernel), then runs the layer."""
+    case = make_case(synth.WORKLOADS["stack48_t1"])  # Zipf bias: all three inputs matter
+    layer = case.layer
+    x = case.x.clone()
+    out = torch.empty_like(x)
+    idx = torch.empty(1, case.wl.k, dtype=torch.int32, device="cuda")
+    ws = binding.workspace(1, layer)
+    srcs = []
+    for step in range(4):
+        wr, b = synth.make_router(case.wl, 10 + step, "cuda")
+        srcs.append((synth.make_x(case.wl, "cuda", step=40 + step), wr, b))
+    nx, nwr, nb = (torch.empty_like(t) for t in srcs[0])
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.layer_forward(x, layer, out=out, ws=ws, idx_out=idx)  # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            x.copy_(nx)
+            layer.router_w.copy_(nwr)
+            layer.router_bias.copy_(nb)
+            binding.layer_forward(x, layer, out=out, ws=ws, idx_out=idx)
+    for sx, swr, sb in srcs:
+        nx.copy_(sx)
+        nwr.copy_(swr)
+        nb.copy_(sb)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref_layer = binding.Layer(case.wl.E, case.wl.k, case.wl.d_model, case.wl.d_ff, layer.gate, layer.up,
+                                  layer.down, swr, sb)
+        ridx = torch.empty_like(idx)
+        ref = binding.layer_forward(sx, ref_layer, idx_out=ridx)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, ridx)
+        assert rel_l2_max(out.double().cpu().numpy(), ref.double().cpu().numpy()) < 1e-6
