@@ -15,12 +15,16 @@
 //      tagged word with no logit (its presence).  Every CTA reads all the
 //      words until each carries its tag -- the logits arrive with them --
 //      then ranks the logits itself (top-k, weights, active experts).  The
-//      tag is a launch counter in the workspace, read by every CTA at its
-//      start and bumped by CTA 0 once every word is in (so every CTA has
-//      read it): nothing needs clearing between launches, and words of
-//      earlier launches carry other tags whatever the workspace held.
+//      tag is a launch counter in the workspace, read by every CTA once the
+//      previous kernel in the stream has completed and bumped by CTA 0 once
+//      every word is in (so every CTA has read it): nothing needs clearing
+//      between launches, and words of earlier launches carry other tags
+//      whatever the workspace held.
 //   2. The routed (expert, feature) units are cut into equal 16-aligned
-//      ranges, one per CTA.  A CTA streams the gate and up rows of its
+//      ranges, one per CTA; the producer warp derives the active experts
+//      and its CTA's range straight from the ranks and starts the weight
+//      stream while the other warps finish the weights and the bucketing.
+//      A CTA streams the gate and up rows of its
 //      features (1-D bulk copies; h = silu(g) * u kept in shared memory) and
 //      then the down-projection COLUMNS of the same features (2-D TMA boxes
 //      of Wd rows x the CTA's columns, with their scales): the down
