@@ -164,6 +164,14 @@ __device__ __forceinline__ void dequant32_q4(uint4 q, f32x2 dd, f32x2 cc, uint32
     v[8] = b0.x, v[9] = b0.y, v[10] = b0.z, v[11] = b0.w, v[12] = b1.x, v[13] = b1.y, v[14] = b1.z, v[15] = b1.w;
 }
 
+// silu(g) * u for the bf16 h of the tensor-core path, with the fast
+// exponential and division intrinsics: their few-ulp errors are far below
+// the bf16 rounding of h that follows (relative 2^-9), and the epilogue is on
+// the gate/up kernel's critical path (its single accumulator buffer waits
+// for it).  For g below about -87 the divisor exceeds 2^126 (or is +inf)
+// and __fdividef gives 0, silu's limit.
+__device__ __forceinline__ float swiglu_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -539,7 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (n < U.nv) {
                         const size_t pp = (size_t)(U.p0 + n);
                         if (EPI == 0) {
-                            p.h[pp * p.rows + U.m0 + row] = __float2bfloat16_rn(silu_f(g[i]) * v[i]);
+                            p.h[pp * p.rows + U.m0 + row] = __float2bfloat16_rn(swiglu_fast(g[i], v[i]));
                         } else if (EPI == 1) {
                             const int tok = s_ep_tok[n];
                             if (tok >= 0) atomicAdd(p.out + (size_t)tok * p.rows + U.m0 + row, s_ep_w[n] * g[i]);
