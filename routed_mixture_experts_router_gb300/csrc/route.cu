@@ -195,17 +195,19 @@ int route_cluster_size(int E, size_t smem) {
 }  // namespace
 
 // ------------------------------------------------------------ large batches
-// Router logits as a split-K fp32 GEMM: one cluster of kGemmCl CTAs per tile
+// Router logits as a split-K fp32 GEMM: one cluster of CL CTAs per tile
 // of kGemmTok tokens; CTA c accumulates K slice c for all experts with 4x EPT
 // register tiles over transposed shared-memory chunks of x and Wr, then the
 // cluster sums the slices through distributed shared memory in a fixed order
 // (deterministic) and each CTA runs the top-k of its share of the tokens.
 constexpr int kGemmTok = 32;
-constexpr int kGemmCl = 8;
+// CL = 16 (a non-portable cluster size, used where the device can
+// co-schedule it): twice the CTAs of CL = 8 over the same tiles, 4-6% off a
+// prefill layer at T = 768-1024
 constexpr int kGemmKc = 32;
 constexpr int kGemmThreads = 256;
 
-template <int EPT>
+template <int EPT, int CL>
 __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ Wr,
                                                                   const float* __restrict__ bias, int T, int dm,
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     const int t0 = blockIdx.y * kGemmTok;
     const int tid = threadIdx.x;
     const int tg = tid & 7, eg = tid >> 3;  // tokens 4tg..4tg+3, experts EPT*eg..
-    const int kslice = dm / kGemmCl;
+    const int kslice = dm / CL;
     const int kbeg = c * kslice;
     const int nch = kslice / kGemmKc;
 
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     cluster.sync();  // every K slice is in its CTA's shared memory
     // CTA c owns tokens c*4 .. c*4+3 of the tile: sum their logits over the
     // K slices in a fixed order (deterministic), then rank them
-    constexpr int kOwn = kGemmTok / kGemmCl;
+    constexpr int kOwn = kGemmTok / CL;
     __shared__ int32_t s_sel[kOwn * MOE_MAX_TOPK];
     __shared__ float s_val[kOwn * MOE_MAX_TOPK];
     float* lg = &xs[0][0];  // reuse: [kOwn][EP] logits (kOwn * EP <= kGemmKc * kGemmTok)
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     for (int i = tid; i < kOwn * EP; i += kGemmThreads) {
         const int tl = c * kOwn + i / EP, e = i % EP;
         float s = 0.f;
-        for (int r = 0; r < kGemmCl; ++r) s += cluster.map_shared_rank(&part[0][0], r)[tl * EP + e];
+        for (int r = 0; r < CL; ++r) s += cluster.map_shared_rank(&part[0][0], r)[tl * EP + e];
         lg[i] = s;
     }
     __syncthreads();
@@ -320,33 +322,72 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     cluster.sync();  // no CTA leaves while others still read its partial sums
 }
 
-template <int EPT>
+template <int EPT, int CL>
 cudaError_t launch_route_gemm(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts,
                               cudaStream_t s) {
+    if (CL > 8) {  // clusters above the portable size must be allowed explicitly
+        const cudaError_t e =
+            cudaFuncSetAttribute(route_gemm_kernel<EPT, CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kGemmCl, (T + kGemmTok - 1) / kGemmTok, 1);
+    cfg.gridDim = dim3(CL, (T + kGemmTok - 1) / kGemmTok, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kGemmCl;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, route_gemm_kernel<EPT>, x, w.router_w, w.router_bias, T, w.d_model, w.E, w.k,
+    return cudaLaunchKernelEx(&cfg, route_gemm_kernel<EPT, CL>, x, w.router_w, w.router_bias, T, w.d_model, w.E, w.k,
                               idx, wts);
+}
+
+// Whether the device co-schedules a 16-CTA cluster of the router GEMM
+// kernel; probed once per process and device (racing first calls store the
+// same answer).
+static bool gemm_cluster16_ok() {
+    static std::atomic<int> cached[64];  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int c = cached[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+        auto kern = route_gemm_kernel<4, 16>;
+        int n = 0;
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(16, 1, 1);
+            cfg.blockDim = dim3(kGemmThreads, 1, 1);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 16;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        }
+        cudaGetLastError();
+        c = (err == cudaSuccess && n > 0) ? 1 : 2;
+        cached[dev].store(c, std::memory_order_relaxed);
+    }
+    return c == 1;
 }
 
 cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* idx, float* wts, int32_t* offsets,
                          int32_t* pair_tok, int32_t* pair_slot, int32_t* pos, bool* bucketed, cudaStream_t s) {
     if (bucketed) *bucketed = false;
     if (T == 0) return cudaSuccess;
-    if (T >= 128 && w.E <= 128 && w.d_model % (kGemmCl * kGemmKc) == 0)
-        return launch_route_gemm<4>(x, T, w, idx, wts, s);
+    if (T >= 128 && w.E <= 128 && w.d_model % (16 * kGemmKc) == 0 && gemm_cluster16_ok())
+        return launch_route_gemm<4, 16>(x, T, w, idx, wts, s);
+    if (T >= 128 && w.E <= 128 && w.d_model % (8 * kGemmKc) == 0)
+        return launch_route_gemm<4, 8>(x, T, w, idx, wts, s);
     // tokens per tile: bounded so the x tile stays within 96 KB of shared memory
     int tt = T >= 8 ? 8 : (T >= 4 ? 4 : (T >= 2 ? 2 : 1));
     while (tt > 1 && (size_t)tt * w.d_model * sizeof(float) > 96 * 1024) tt >>= 1;
