@@ -42,7 +42,11 @@
  *
  * Device weight layout, Q8_0 (moe_layer_w.wfmt = MOE_WFMT_Q8_0, produced by
  * moe_pack_q8 from the 34-byte blocks):
- *   qs  int8     [E][rows][K]       the 32 int8 values of each block, along K
+ *   qs  bytes    [E][rows][K]       the 32 int8 values q of each block, along
+ *                                   K, each stored as the byte q + 128 (its
+ *                                   sign bit flipped: offset binary), the
+ *                                   form the exact dequantisation takes; the
+ *                                   weight is (u - 128) * d
  *   d   fp16 bits[E][rows][K/32]    one scale per 32-wide block
  * Q4_0 (MOE_WFMT_Q4_0, produced by moe_pack_q4 from 18-byte blocks):
  *   qs  bytes    [E][rows][K/2]     each block's 16 bytes, unchanged: byte j
@@ -150,8 +154,9 @@ MOE_API size_t moe_workspace_size(int T, const moe_layer_w* w, int act, int flag
  * Repack Q8_0 weights from the pages' 34-byte blocks (fp16 scale d, little
  * endian, then 32 int8 values q along K) into the device layout.
  *   blocks: device bytes, rows * (K/32) blocks, row-major (any alignment)
- *   qs: int8 [rows][K] (16-byte aligned); d: fp16 bits [rows][K/32]
- * rows may span several experts ([E*rows_per_expert]).  Bit-exact copy.
+ *   qs: bytes q + 128 [rows][K] (16-byte aligned); d: fp16 bits [rows][K/32]
+ * rows may span several experts ([E*rows_per_expert]).  Exact: the scale
+ * bits are copied and each value's sign bit is flipped.
  */
 MOE_API int moe_pack_q8(const uint8_t* blocks, long long rows, int K, int8_t* qs, uint16_t* d, void* stream);
 

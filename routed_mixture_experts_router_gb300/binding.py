@@ -132,7 +132,7 @@ def _check(fn: str, rc: int):
 class Layer:
     """Device-resident weights of one MoE layer in the library's layout.
 
-    Holds the packed expert tensors (Q8_0: qs int8 [E][rows][K]; Q4_0: qs
+    Holds the packed expert tensors (Q8_0: qs [E][rows][K], bytes q + 128; Q4_0: qs
     uint8 [E][rows][K/2]; d fp16-bits [E][rows][K/32]) and the fp32 router,
     plus the C struct pointing at them.  wfmt: MOE_WFMT_Q8_0 or MOE_WFMT_Q4_0.
     """
@@ -171,7 +171,7 @@ def version() -> str:
 
 
 def pack_q8(blocks: torch.Tensor, rows: int, K: int):
-    """moe_pack_q8: 34-byte blocks -> (qs int8 [rows][K], d int16-bits [rows][K/32])."""
+    """moe_pack_q8: 34-byte blocks -> (qs [rows][K] holding q + 128 as bytes, d int16-bits [rows][K/32])."""
     L = load()
     qs = torch.empty(rows, K, dtype=torch.int8, device=blocks.device)
     d = torch.empty(rows, K // 32, dtype=torch.int16, device=blocks.device)

@@ -42,12 +42,12 @@ __device__ __forceinline__ float ldg_half(const uint16_t* p) {
     return __half2float(__ushort_as_half(b));
 }
 
-// Four int8 values packed in a 32-bit word -> four exact fp32 values.
-// Each byte is biased to unsigned (xor 0x80), placed in the low mantissa byte
-// of 2^23 (0x4B0000uu = 8388608 + u), and the bias 8388608 + 128 is
-// subtracted; every step is exact.
+// Four Q8_0 values in a 32-bit word of the device layout (bytes u = q + 128)
+// -> four exact fp32 values q: each byte goes into the low mantissa byte of
+// 2^23 (0x4B0000uu = 8388608 + u) and 8388608 + 128 is subtracted; every
+// step is exact.
 __device__ __forceinline__ float4 i8x4_to_f32x4(uint32_t w) {
-    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t u = w;
     float4 r;
     r.x = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
     r.y = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;

@@ -142,11 +142,11 @@ __device__ __forceinline__ void chunk_fma_u(const uint32_t (&words)[4], float d,
     }
 }
 
-// Q8_0: one 16-byte chunk of 16 int8 values.
+// Q8_0: one 16-byte chunk of 16 values (device layout: bytes u = q + 128).
 template <int TT>
 __device__ __forceinline__ void chunk_fma(const uint4 q, float d, const float4* const (&xt)[TT], int st,
                                           f32x2 (&acc)[TT][2]) {
-    const uint32_t u[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};  // bytes u = q + 128 (device layout)
     chunk_fma_u<TT>(u, d, 128.0f, xt, st, acc);
 }
 

@@ -144,9 +144,9 @@ __device__ __forceinline__ void dequant16_u(const uint32_t (&w)[4], f32x2 dd, f3
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// Q8_0: 16 int8 values of one block (one 16-byte word), bytes offset by 128.
+// Q8_0: 16 values of one block (one 16-byte word of the device layout: bytes u = q + 128).
 __device__ __forceinline__ void dequant16(uint4 q, f32x2 dd, f32x2 cc, uint4& o0, uint4& o1) {
-    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};  // bytes u = q + 128 (device layout)
     dequant16_u(w, dd, cc, o0, o1);
 }
 

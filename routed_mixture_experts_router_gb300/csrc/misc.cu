@@ -7,7 +7,9 @@ namespace {
 
 // One thread per 34-byte block: fp16 scale (little endian) then 32 int8
 // values (amalgafy.com/technical-overview, "Validated GPU foundation":
-// native Q8_0 weights).  Bytes are copied unchanged into the split layout.
+// native Q8_0 weights).  The scale is copied unchanged; each value q is
+// stored as the byte q + 128 (its sign bit flipped: offset binary), the form
+// every kernel's exact dequantisation takes directly.
 __global__ void pack_q8_kernel(const uint8_t* __restrict__ blocks, long long nblocks, int8_t* __restrict__ qs,
                                uint16_t* __restrict__ d) {
     const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -17,8 +19,9 @@ __global__ void pack_q8_kernel(const uint8_t* __restrict__ blocks, long long nbl
     uint32_t wv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        wv[i] = (uint32_t)src[2 + 4 * i] | ((uint32_t)src[3 + 4 * i] << 8) | ((uint32_t)src[4 + 4 * i] << 16) |
-                ((uint32_t)src[5 + 4 * i] << 24);
+        wv[i] = ((uint32_t)src[2 + 4 * i] | ((uint32_t)src[3 + 4 * i] << 8) | ((uint32_t)src[4 + 4 * i] << 16) |
+                 ((uint32_t)src[5 + 4 * i] << 24)) ^
+                0x80808080u;  // q -> q + 128 in every byte
     uint4* dst = reinterpret_cast<uint4*>(qs + b * 32);
     dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);

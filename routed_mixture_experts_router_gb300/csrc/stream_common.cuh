@@ -48,7 +48,7 @@ __device__ __forceinline__ void dequant16(const uint4 q, float d, f32x2 (&w)[8])
     const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const uint32_t u = words[m] ^ 0x80808080u;
+        const uint32_t u = words[m];  // bytes u = q + 128 (device layout)
         w[2 * m] = f2_fma(f2_pack(__uint_as_float(__byte_perm(u, 0x47000000u, 0x7504)),
                                   __uint_as_float(__byte_perm(u, 0x47000000u, 0x7514))),
                           dd, cc);

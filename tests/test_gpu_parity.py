@@ -51,7 +51,8 @@ def test_pack_q8_bit_exact():
     blocks = synth.quantize_q8_0(w)
     qs, d = binding.pack_q8(blocks, 37, 96)
     b = blocks.cpu().numpy().reshape(37, 3, 34)
-    assert np.array_equal(qs.cpu().numpy().reshape(37, 3, 32).view(np.uint8), b[:, :, 2:])
+    # device layout: each int8 value q as the byte q + 128 (sign bit flipped)
+    assert np.array_equal(qs.cpu().numpy().reshape(37, 3, 32).view(np.uint8), b[:, :, 2:] ^ 0x80)
     assert np.array_equal(d.cpu().numpy().view(np.uint8).reshape(37, 3, 2), b[:, :, :2])
 
 
