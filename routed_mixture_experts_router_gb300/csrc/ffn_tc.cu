@@ -578,21 +578,24 @@ __global__ void gather_bf16_kernel(const float* __restrict__ x, int T, int dm, c
     pdl_wait();
     pdl_launch_dependents();
     const int pv = __ldcg(offsets + E);
-    const int c8 = dm / 8;
-    const size_t n = (size_t)P * c8;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const int pp = (int)(i / c8), c = (int)(i - (size_t)pp * c8);
-        uint4 o = make_uint4(0, 0, 0, 0);
+    const int c8 = dm / 8;  // 16-byte output chunks per row
+    // one warp per pair row: lane c converts 8 values (two float4 of x) into
+    // one 16-byte chunk, consecutive lanes on consecutive chunks
+    const int lane = threadIdx.x & 31;
+    const int nw = (int)(gridDim.x * blockDim.x) >> 5;
+    for (int pp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); pp < P; pp += nw) {
         const int t = pp < pv ? __ldcg(pair_tok + pp) : -1;
+        uint4* dst = reinterpret_cast<uint4*>(xb) + (size_t)pp * c8;
         if (t >= 0 && t < T) {
-            const float4* src = reinterpret_cast<const float4*>(x + (size_t)t * dm) + 2 * c;
-            const float4 a = __ldcg(src), b = __ldcg(src + 1);
-            o.x = bf16x2_rn(a.x, a.y);
-            o.y = bf16x2_rn(a.z, a.w);
-            o.z = bf16x2_rn(b.x, b.y);
-            o.w = bf16x2_rn(b.z, b.w);
+            const float4* src = reinterpret_cast<const float4*>(x + (size_t)t * dm);
+            for (int c = lane; c < c8; c += 32) {
+                const float4 a = __ldcg(src + 2 * c), b = __ldcg(src + 2 * c + 1);
+                dst[c] = make_uint4(bf16x2_rn(a.x, a.y), bf16x2_rn(a.z, a.w), bf16x2_rn(b.x, b.y),
+                                    bf16x2_rn(b.z, b.w));
+            }
+        } else {
+            for (int c = lane; c < c8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
         }
-        reinterpret_cast<uint4*>(xb)[i] = o;
     }
     if (out_init) {
         const size_t n4 = (size_t)T * dm / 4;
