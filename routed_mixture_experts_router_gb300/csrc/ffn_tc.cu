@@ -326,7 +326,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         prefetch_tmap(&tm_b);
     }
-    pdl_wait();  // bucketing and the previous stage's activations are complete
+    // Only the token producer reads what the previous kernel in the stream
+    // wrote (the gathered bf16 x, or h).  The weights, the bucketing, the
+    // routing weights, the arena's slots and the initialised out were all
+    // complete before that kernel could start (it waits for its own
+    // predecessor before it lets this grid launch), so the active experts,
+    // the weight stream and its dequantisation start at once, overlapping
+    // the previous kernel's tail.
     if (warp == 2) tc_build_active(p.offsets, p.E, p.T * p.k, s_act, s_beg, s_end, s_cb, &s_n, p.eslot, p.nslots);
     tc_fence_before();
     __syncthreads();
@@ -370,6 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 2) {
         // ------------------------------------------------- TMA producer: tokens
         if (lane == 0) {
+            pdl_wait();  // the previous kernel's activations are complete and visible
             uint32_t ac = 0;
             for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
                 const Unit U = decode_unit(u, mt, s_act, s_beg, s_end, s_cb, s_n, p.band);
