@@ -118,12 +118,12 @@ int check_device() {
 cudaError_t launch_ffn(const float* x, int T, const moe_layer_w& w, int act, const int32_t* offsets,
                        const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse, float* out,
                        int residual, char* ws, const WsLayout& L, int32_t* status, cudaStream_t s,
-                       int reuse_order = 0) {
+                       int reuse_order = 0, int in_layer = 0) {
     float* h = reinterpret_cast<float*>(ws + L.h);
     if (act == MOE_ACT_BF16 && ffn_tc_supported(w, T))
         return launch_ffn_tc(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual,
                              reinterpret_cast<__nv_bfloat16*>(ws + L.xb), reinterpret_cast<__nv_bfloat16*>(h),
-                             status, reuse_order, s);
+                             status, reuse_order, in_layer, s);
     if (w.wfmt != MOE_WFMT_Q8_0) {
         if (!ffn_rows_supported(w, T)) return cudaErrorNotSupported;
         return launch_ffn_rows(x, T, w, offsets, pair_tok, pair_slot, wts, fuse, out, residual, h, s);
@@ -174,11 +174,11 @@ cudaError_t layer_chain(const float* x, int T, const moe_layer_w& w, int act, in
     const int ro = (flags & MOE_FLAG_REUSE_ORDER) ? 1 : 0;
     if (flags & MOE_FLAG_DETERMINISTIC) {
         float* yp = reinterpret_cast<float*>(base + L.ypairs);
-        e = launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 0, yp, 0, base, L, status, s, ro);
+        e = launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 0, yp, 0, base, L, status, s, ro, 1);
         if (e != cudaSuccess) return e;
         return launch_combine(yp, wts, pos, T, w.k, w.d_model, residual ? x : nullptr, out, s);
     }
-    return launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 1, out, residual, base, L, status, s, ro);
+    return launch_ffn(x, T, wf, act, off, ptok, pslot, wts, 1, out, residual, base, L, status, s, ro, 1);
 }
 
 }  // namespace

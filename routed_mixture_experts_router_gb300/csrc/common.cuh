@@ -108,11 +108,14 @@ cudaError_t launch_ffn_stream(const float* x, int T, const moe_layer_w& w, const
                               float* out_or_ypairs, int residual, float* h, int32_t* status, cudaStream_t s);
 
 // Tensor-core (tcgen05) bf16 expert path for prefill-size batches.
+// in_layer: the preceding kernel in the stream is this library's routing,
+// bucketing or arena admission of the same layer call (none of them reads or
+// writes out), so out may be initialised before that kernel completes.
 bool ffn_tc_supported(const moe_layer_w& w, int T);
 cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                           const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                           float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
-                          int reuse_order, cudaStream_t s);
+                          int reuse_order, int in_layer, cudaStream_t s);
 
 // The whole layer for T <= 2 decode tokens in one cooperative launch (fp32
 // path).  logits: [T][E] scratch; h: [T*k][d_ff] scratch; sync: 2 words.

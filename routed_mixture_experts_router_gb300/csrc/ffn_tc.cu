@@ -581,9 +581,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // out = residual ? x : 0 for the down kernel's atomics.
 __global__ void gather_bf16_kernel(const float* __restrict__ x, int T, int dm, const int32_t* __restrict__ pair_tok,
                                    const int32_t* __restrict__ offsets, int E, int P, __nv_bfloat16* __restrict__ xb,
-                                   float* __restrict__ out_init, int residual) {
-    pdl_wait();
+                                   float* __restrict__ out_init, int residual, int init_early) {
+    // The combine target first when the preceding kernel is this library's
+    // routing, bucketing or arena admission of the same call: none of them
+    // writes x or reads or writes out (out never aliases x), and every
+    // kernel before them was complete before they let this grid launch, so
+    // out is initialised while they still run.
+    if (out_init && init_early) {
+        const size_t n4 = (size_t)T * dm / 4;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+            reinterpret_cast<float4*>(out_init)[i] =
+                residual ? __ldcg(reinterpret_cast<const float4*>(x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();  // the bucketing (pair_tok, offsets) is complete
     pdl_launch_dependents();
+    if (out_init && !init_early) {
+        const size_t n4 = (size_t)T * dm / 4;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+            reinterpret_cast<float4*>(out_init)[i] =
+                residual ? __ldcg(reinterpret_cast<const float4*>(x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const int pv = __ldcg(offsets + E);
     const int c8 = dm / 8;  // 16-byte output chunks per row
     // one warp per pair row: lane c converts 8 values (two float4 of x) into
@@ -603,12 +620,6 @@ __global__ void gather_bf16_kernel(const float* __restrict__ x, int T, int dm, c
         } else {
             for (int c = lane; c < c8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
         }
-    }
-    if (out_init) {
-        const size_t n4 = (size_t)T * dm / 4;
-        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
-            reinterpret_cast<float4*>(out_init)[i] =
-                residual ? __ldcg(reinterpret_cast<const float4*>(x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -688,7 +699,7 @@ bool ffn_tc_supported(const moe_layer_w& w, int T) {
 cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int32_t* offsets,
                           const int32_t* pair_tok, const int32_t* pair_slot, const float* wts, int fuse_combine,
                           float* out_or_ypairs, int residual, __nv_bfloat16* xb, __nv_bfloat16* hb, int32_t* status,
-                          int reuse_order, cudaStream_t s) {
+                          int reuse_order, int in_layer, cudaStream_t s) {
     const int P = T * w.k;
     const int dm = w.d_model, f = w.d_ff;
     {
@@ -702,7 +713,7 @@ cudaError_t launch_ffn_tc(const float* x, int T, const moe_layer_w& w, const int
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaError_t err = cudaLaunchKernelEx(&cfg, gather_bf16_kernel, x, T, dm, pair_tok, offsets, w.E, P, xb,
-                                             fuse_combine ? out_or_ypairs : (float*)nullptr, residual);
+                                             fuse_combine ? out_or_ypairs : (float*)nullptr, residual, in_layer);
         if (err != cudaSuccess) return err;
     }
     CUtensorMap tg, tu, td, txb, th, sg, su, sd;
