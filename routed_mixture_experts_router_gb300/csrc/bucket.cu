@@ -23,6 +23,63 @@ namespace moe {
 
 namespace {
 
+// Token t's k expert ids, each valid id (in [0, E)) kept at its first
+// occurrence: keep(s, e) for every kept slot s; *bad set when an id is out of
+// range or repeats.  k <= 8 (the common top-k): the ids in registers (two
+// 16-byte loads when aligned), each compared with the token's earlier slots;
+// larger k: a bitmap over the experts.
+template <class Keep>
+__device__ __forceinline__ void token_ids(const int32_t* __restrict__ idx, int t, int k, int E, int* bad,
+                                          Keep keep) {
+    if (k <= 8) {
+        int ids[8];
+        const int32_t* row = idx + (size_t)t * k;
+        if (k == 8 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+            const int4 a = __ldcg(reinterpret_cast<const int4*>(row)), b = __ldcg(reinterpret_cast<const int4*>(row) + 1);
+            ids[0] = a.x, ids[1] = a.y, ids[2] = a.z, ids[3] = a.w, ids[4] = b.x, ids[5] = b.y, ids[6] = b.z, ids[7] = b.w;
+        } else {
+#pragma unroll
+            for (int s = 0; s < 8; ++s) ids[s] = s < k ? __ldcg(row + s) : -1;
+        }
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            if (s >= k) break;
+            const int e = ids[s];
+            bool ok = e >= 0 && e < E;
+#pragma unroll
+            for (int s3 = 0; s3 < s; ++s3) ok = ok && ids[s3] != e;
+            if (!ok) {
+                *bad = 1;
+                continue;
+            }
+            keep(s, e);
+        }
+        return;
+    }
+    uint32_t seen[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) seen[j] = 0;
+    for (int s = 0; s < k; ++s) {
+        const int e = __ldcg(idx + (size_t)t * k + s);
+        bool ok = e >= 0 && e < E;
+        if (ok) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                if (j == (e >> 5)) word = seen[j];
+            ok = !(word & (1u << (e & 31)));
+#pragma unroll
+            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
+                if (j == (e >> 5)) seen[j] |= 1u << (e & 31);
+        }
+        if (!ok) {
+            *bad = 1;
+            continue;
+        }
+        keep(s, e);
+    }
+}
+
 constexpr int kBucketThreads = 1024;
 constexpr int kBucketWarps = kBucketThreads / kWarp;
 
@@ -54,36 +111,10 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
 
     // 1. counts (valid ids only; a repeated id within a token is dropped below
     //    and not counted: rows with repeats are detected per token)
-    for (int t = tid; t < T; t += kBucketThreads) {
-        uint32_t bm[MOE_MAX_EXPERTS / 32];
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) bm[j] = 0;
-        int ids[MOE_MAX_TOPK];  // all of the token's ids in one round trip
-#pragma unroll
-        for (int s = 0; s < MOE_MAX_TOPK; ++s) ids[s] = s < k ? __ldcg(idx + (size_t)t * k + s) : -1;
-#pragma unroll
-        for (int s = 0; s < MOE_MAX_TOPK; ++s) {
-            if (s >= k) break;
-            const int e = ids[s];
-            if (e < 0 || e >= E) {
-                s_bad = 1;
-                continue;
-            }
-            const uint32_t bit = 1u << (e & 31);
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                if (j == (e >> 5)) word = bm[j];
-            if (word & bit) {
-                s_bad = 1;
-                continue;
-            }
-#pragma unroll
-            for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                if (j == (e >> 5)) bm[j] |= bit;
-            atomicAdd(&s_cnt[e], 1);
-        }
-    }
+    int bad = 0;
+    for (int t = tid; t < T; t += kBucketThreads)
+        token_ids(idx, t, k, E, &bad, [&](int, int e) { atomicAdd(&s_cnt[e], 1); });
+    if (bad) s_bad = 1;
     __syncthreads();
     // exclusive scan over E <= 256 counts: warps 0..7 scan 32 each, then fix up
     if (tid < MOE_MAX_EXPERTS) {
@@ -212,36 +243,13 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_mask_kernel(const int32
     __syncthreads();
 
     // 1. one token per thread: validate its ids, drop repeats, set the bits
-    for (int t = tid; t < T; t += kBucketThreads) {
-        uint32_t seen[MOE_MAX_EXPERTS / 32];
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) seen[j] = 0;
-        int ids[MOE_MAX_TOPK];
-#pragma unroll
-        for (int s = 0; s < MOE_MAX_TOPK; ++s) ids[s] = s < k ? __ldcg(idx + (size_t)t * k + s) : -1;
-#pragma unroll
-        for (int s = 0; s < MOE_MAX_TOPK; ++s) {
-            if (s >= k) break;
-            const int e = ids[s];
-            bool ok = e >= 0 && e < E;
-            if (ok) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                    if (j == (e >> 5)) word = seen[j];
-                ok = !(word & (1u << (e & 31)));
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                    if (j == (e >> 5)) seen[j] |= 1u << (e & 31);
-            }
-            if (!ok) {
-                s_bad = 1;
-                continue;
-            }
+    int bad = 0;
+    for (int t = tid; t < T; t += kBucketThreads)
+        token_ids(idx, t, k, E, &bad, [&](int s, int e) {
             const int p = t * k + s;
             atomicOr(&s_mask[(size_t)e * W + (p >> 5)], 1u << (p & 31));
-        }
-    }
+        });
+    if (bad) s_bad = 1;
     __syncthreads();
     // 2. per expert (one warp each): word prefix counts and the bucket size
     for (int e = warp; e < E; e += kBucketWarps) {
@@ -337,32 +345,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_tiles_kernel(const int3
     __syncthreads();
 
     // 1. every token: validate, drop repeats; count; set this tile's bits
-    for (int t = tid; t < T; t += kBucketThreads) {
-        uint32_t seen[MOE_MAX_EXPERTS / 32];
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) seen[j] = 0;
-        int ids[MOE_MAX_TOPK];
-#pragma unroll
-        for (int s2 = 0; s2 < MOE_MAX_TOPK; ++s2) ids[s2] = s2 < k ? __ldcg(idx + (size_t)t * k + s2) : -1;
-#pragma unroll
-        for (int s2 = 0; s2 < MOE_MAX_TOPK; ++s2) {
-            if (s2 >= k) break;
-            const int e = ids[s2];
-            bool ok = e >= 0 && e < E;
-            if (ok) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                    if (j == (e >> 5)) word = seen[j];
-                ok = !(word & (1u << (e & 31)));
-#pragma unroll
-                for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j)
-                    if (j == (e >> 5)) seen[j] |= 1u << (e & 31);
-            }
-            if (!ok) {
-                s_bad = 1;
-                continue;
-            }
+    int bad = 0;
+    for (int t = tid; t < T; t += kBucketThreads)
+        token_ids(idx, t, k, E, &bad, [&](int s2, int e) {
             atomicAdd(&s_total[e], 1);
             if (t < t0) {
                 atomicAdd(&s_before[e], 1);
@@ -370,8 +355,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_tiles_kernel(const int3
                 const int q = (t - t0) * k + s2;
                 atomicOr(&s_mask[e * kTileWords + (q >> 5)], 1u << (q & 31));
             }
-        }
-    }
+        });
+    if (bad) s_bad = 1;
     __syncthreads();
     // 2. offsets (exclusive scan of the totals) and the tile's word prefixes
     if (tid < MOE_MAX_EXPERTS) {
