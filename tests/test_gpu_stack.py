@@ -40,7 +40,9 @@ def _stack_chain(name, nlayers, tokens=None, tol=TOL_F32, final_tol=None):
       layer's error is measured alone (the MoE part x_{l+1} - x_l against
       the oracle's MoE output, max relative L2 over tokens <= tol);
     * free-running: the oracle's own chain from the same x_0, compared with
-      the GPU's final hidden state (max relative L2 <= final_tol).
+      the GPU's final hidden state (max relative L2 <= final_tol, by default
+      the sum of the per-layer errors: the rounding each layer injects adds
+      up through the residual stream).
 
     The bf16 path is gated against the plain oracle on fp32 inputs; the
     error against the oracle fed bf16-rounded expert inputs is printed as a
@@ -111,7 +113,13 @@ def _stack_chain(name, nlayers, tokens=None, tol=TOL_F32, final_tol=None):
         print(f"{name}: diagnostic, against the oracle on bf16-rounded expert inputs: max {max(errs_bf):.2e}")
     print(f"{name}: final hidden state vs the oracle's own chain: max rel L2 {final:.2e}; "
           f"near-tie tokens {near_total}, free-running selections taken from the GPU {flips}")
-    assert final < (tol if final_tol is None else final_tol), f"final hidden state max rel L2 {final:.3e}"
+    # Each layer injects its own rounding (its teacher-forced error, each
+    # within tol); through the residual stream x_{l+1} = x_l + MoE_l(x_l)
+    # those errors add up to first order, so the free-running final state is
+    # bounded by their sum (not by one layer's tol: 48 fp32 layers measured
+    # 0.9-1.05e-5 against per-layer errors of 7-9e-7 that sum to ~4e-5).
+    bound = final_tol if final_tol is not None else max(tol, float(np.sum(errs)))
+    assert final < bound, f"final hidden state max rel L2 {final:.3e} (bound {bound:.3e})"
     return errs, final
 
 
