@@ -390,14 +390,14 @@ cudaError_t launch_route(const float* x, int T, const moe_layer_w& w, int32_t* i
     // 16-CTA clusters (twice the CTAs per token tile) where every tile's
     // cluster is resident at once; else 8-CTA clusters, which fit twice as
     // many at a time (T = 2048: 46.5 instead of 50.3 us)
-    if (T >= 128 && w.E <= 128 && w.d_model % (16 * kGemmKc) == 0) {
+    if (T >= 64 && w.E <= 128 && w.d_model % (16 * kGemmKc) == 0) {
         const int tiles = (T + kGemmTok - 1) / kGemmTok;
         const int n16 = gemm_max_clusters<16>(), n8 = gemm_max_clusters<8>();
         const int waves16 = n16 > 0 ? (tiles + n16 - 1) / n16 : INT_MAX;
         const int waves8 = n8 > 0 ? (tiles + n8 - 1) / n8 : INT_MAX;
         if (n16 > 0 && waves16 <= waves8) return launch_route_gemm<4, 16>(x, T, w, idx, wts, s);
     }
-    if (T >= 128 && w.E <= 128 && w.d_model % (8 * kGemmKc) == 0)
+    if (T >= 64 && w.E <= 128 && w.d_model % (8 * kGemmKc) == 0)
         return launch_route_gemm<4, 8>(x, T, w, idx, wts, s);
     // tokens per tile: bounded so the x tile stays within 96 KB of shared
     // memory; several tiles of 4 rather than 8 tokens (twice the clusters
