@@ -135,6 +135,45 @@ def test_bucket_bad_ids_many_tiles():
     assert np.array_equal(ps.cpu().numpy()[:n], [p[2] for p in pairs])
 
 
+@pytest.mark.parametrize("T,k,E", [(300, 8, 128), (100, 8, 128), (200, 12, 64), (50, 12, 64)])
+def test_bucket_repeats_both_id_checks(T, k, E):
+    """Invalid and repeated ids at k = 8 (ids in registers, 16-byte loads) and
+    k = 12 (a bitmap over the experts), through the many-CTA kernel (T k >=
+    2048 pairs) and the single-CTA one: the first occurrence of a valid id is
+    kept, later repeats and out-of-range ids dropped (pos -1) and flagged."""
+    rng = np.random.default_rng(T * 131 + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    r = rng.random((T, k))
+    idx[r < 0.02] = -3
+    idx[(r >= 0.02) & (r < 0.04)] = E
+    for t in range(0, T, 7):                        # a repeat in every seventh token
+        s_from, s_to = sorted(rng.choice(k, 2, replace=False))
+        idx[t, s_to] = idx[t, s_from]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    off, pt, ps, pos = binding.bucket(torch.from_numpy(idx).cuda(), E, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & binding.MOE_STATUS_BAD_INDEX
+    pairs = []
+    for t in range(T):
+        seen = set()
+        for s in range(k):
+            e = int(idx[t, s])
+            if 0 <= e < E and e not in seen:
+                pairs.append((e, t, s))
+            if 0 <= e < E:
+                seen.add(e)
+    pairs.sort()
+    exp_pos = -np.ones(T * k, dtype=np.int64)
+    for rank, (_, t, s) in enumerate(pairs):
+        exp_pos[t * k + s] = rank
+    assert np.array_equal(off.cpu().numpy(),
+                          np.searchsorted(np.array([q[0] for q in pairs]), np.arange(E + 1), side="left"))
+    assert np.array_equal(pos.cpu().numpy(), exp_pos)
+    n = len(pairs)
+    assert np.array_equal(pt.cpu().numpy()[:n], [q[1] for q in pairs])
+    assert np.array_equal(ps.cpu().numpy()[:n], [q[2] for q in pairs])
+
+
 def test_bucket_bad_ids_flag_status():
     idx = torch.tensor([[0, 1], [5, 5], [2, 99], [-1, 3]], dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
