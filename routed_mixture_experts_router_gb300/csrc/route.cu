@@ -198,9 +198,10 @@ int route_cluster_size(int E, size_t smem) {
 // ------------------------------------------------------------ large batches
 // Router logits as a split-K fp32 GEMM: one cluster of CL CTAs per tile
 // of kGemmTok tokens; CTA c accumulates K slice c for all experts with 4x EPT
-// register tiles over transposed shared-memory chunks of x and Wr, then the
-// cluster sums the slices through distributed shared memory in a fixed order
-// (deterministic) and each CTA runs the top-k of its share of the tokens.
+// register tiles over transposed shared-memory chunks of x and Wr, then
+// pushes each token's slice into the shared memory of the CTA that owns the
+// token (distributed shared memory, one cluster barrier); the owner sums the
+// slices in a fixed order (deterministic) and runs the top-k of its tokens.
 constexpr int kGemmTok = 32;
 // CL = 16 (a non-portable cluster size, used where the device can
 // co-schedule it): twice the CTAs of CL = 8 over the same tiles, 4-6% off a
@@ -249,6 +250,8 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     };
     // column `col` of k row `kr` lives at swz(col, kr)
     auto swz = [](int col, int kr) { return (((col >> 2) ^ ((kr >> 2) & 7)) << 2) | (col & 3); };
+    // this CTA has started: its receive buffer may be written by the others
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_wait();  // x is written by earlier kernels
     load(0);
     float acc[4][EPT];
@@ -292,14 +295,29 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
                 for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xa[i], wv[j], acc[i][j]);
         }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) part[tg * 4 + i][eg * EPT + j] = acc[i][j];
-    cluster.sync();  // every K slice is in its CTA's shared memory
-    // CTA c owns tokens c*4 .. c*4+3 of the tile: sum their logits over the
-    // K slices in a fixed order (deterministic), then rank them
+    // CTA c owns tokens c*kOwn .. c*kOwn+kOwn-1 of the tile; part, in the
+    // owner, receives slice r of its token tl at row r*kOwn + tl
     constexpr int kOwn = kGemmTok / CL;
+    static_assert(EPT % 4 == 0, "vector pushes");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster has started
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int tt = tg * 4 + i, owner = tt / kOwn, tl = tt - owner * kOwn;
+#pragma unroll
+        for (int j = 0; j < EPT; j += 4) {
+            uint32_t a;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                         : "=r"(a)
+                         : "r"(smem_u32(&part[c * kOwn + tl][eg * EPT + j])), "r"(owner));
+            asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(acc[i][j]),
+                         "f"(acc[i][j + 1]), "f"(acc[i][j + 2]), "f"(acc[i][j + 3])
+                         : "memory");
+        }
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every slice of this CTA's tokens is in
+    // sum the owned tokens' logits over the K slices in a fixed order
+    // (deterministic), then rank them
     __shared__ int32_t s_sel[kOwn * MOE_MAX_TOPK];
     __shared__ float s_val[kOwn * MOE_MAX_TOPK];
     float* lg = &xs[0][0];  // reuse: [kOwn][EP] logits (kOwn * EP <= kGemmKc * kGemmTok)
@@ -308,7 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
     for (int i = tid; i < kOwn * EP; i += kGemmThreads) {
         const int tl = c * kOwn + i / EP, e = i % EP;
         float s = 0.f;
-        for (int r = 0; r < CL; ++r) s += cluster.map_shared_rank(&part[0][0], r)[tl * EP + e];
+        for (int r = 0; r < CL; ++r) s += part[r * kOwn + (tl - c * kOwn)][e];
         lg[i] = s;
     }
     __syncthreads();
@@ -320,7 +338,6 @@ __global__ void __launch_bounds__(kGemmThreads) route_gemm_kernel(const float* _
         idx[(size_t)tb * k + q] = s_sel[q];
         wts[(size_t)tb * k + q] = topk_weight(s_val, q, k);
     }
-    cluster.sync();  // no CTA leaves while others still read its partial sums
 }
 
 template <int EPT, int CL>
