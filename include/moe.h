@@ -243,8 +243,12 @@ MOE_API int moe_combine(const float* ypairs, const float* wts, const int32_t* po
  * everything it reads that a previous kernel may have written (x, the
  * weights, the workspace) is read after that kernel has completed.
  * Otherwise router, bucketing and the expert kernels (tcgen05 for
- * MOE_ACT_BF16 with >= 128 pairs).  Grid exchanges and mbarrier waits are
- * bounded (MOE_STATUS_TIMEOUT).
+ * MOE_ACT_BF16 with >= 128 pairs), each a programmatic dependent of the one
+ * before: the first reads x only after the caller's previous kernel has
+ * completed, and a later one reads early only what an earlier kernel of the
+ * same call was done with before it let that one launch (the tcgen05
+ * kernels stream weights while the previous kernel of the call finishes).
+ * Grid exchanges and mbarrier waits are bounded (MOE_STATUS_TIMEOUT).
  *   act: MOE_ACT_F32 or MOE_ACT_BF16; flags: MOE_FLAG_*
  *   residual: 1 adds x to the output (a residual stream between layers)
  *   idx_out [T][k], wts_out [T][k], offsets_out [E+1]: optional copies of the
