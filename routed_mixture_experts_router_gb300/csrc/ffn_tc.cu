@@ -326,13 +326,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         prefetch_tmap(&tm_b);
     }
-    // Only the token producer reads what the previous kernel in the stream
-    // wrote (the gathered bf16 x, or h).  The weights, the bucketing, the
-    // routing weights, the arena's slots and the initialised out were all
-    // complete before that kernel could start (it waits for its own
-    // predecessor before it lets this grid launch), so the active experts,
-    // the weight stream and its dequantisation start at once, overlapping
-    // the previous kernel's tail.
+    // Only the token producer waits for the previous kernel in the stream:
+    // it alone reads what that kernel wrote (the gathered bf16 x, or h).
+    // The weights, the bucketing, the routing weights and the arena's slots
+    // were complete before that kernel let this grid launch (it waits for
+    // its own predecessor first), so the active experts, the weight stream
+    // and its dequantisation start at once, overlapping the previous
+    // kernel's tail.  The combine target out is touched only by the down
+    // projection's epilogue, after MMAs that follow the token producer's
+    // wait (by then every kernel before this one has completed).
     if (warp == 2) tc_build_active(p.offsets, p.E, p.T * p.k, s_act, s_beg, s_end, s_cb, &s_n, p.eslot, p.nslots);
     tc_fence_before();
     __syncthreads();
